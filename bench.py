@@ -1,0 +1,376 @@
+#!/usr/bin/env python
+"""KDA benchmark on GB300: prefill tokens/s and decode steps/s (H=96, d=128)
+as absolute throughput and as a fraction of the HBM roofline.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl kda|reference]
+
+One JSON line on stdout (rank 0).  The headline `value` is prefill tokens/s
+on the single-sequence workload (T=4096, H=96, d_k=d_v=128, bf16 q/k/v, fp32
+g/beta/state); the same line carries the decode workload (256 sequences x one
+token) and the long-context workload (T=262,144 through the fused prologue
+and the prefill) as sub-objects, each with its own roofline.
+
+Timing: W untimed warm-up steps, then exactly K steps bracketed by a barrier
+and a device synchronise on both sides, CUDA events on the launching stream,
+max over ranks.  Every workload's inputs exceed the 129 MB L2 (no flush).
+With N > 1 (torchrun) every rank runs its own copy of the workload on its GPU
+(independent sequences, no collective on the data path): weak scaling.
+
+--impl reference times the fp64 CPU oracle (the only implementation the
+pages leave to compare against) on the host cores, on a bounded head sample
+of the same workload, and prints the same line with "impl": "reference".
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+METRIC = "KDA prefill tokens/s and decode steps/s (H=96,d=128), % of roofline"
+H, D = 96, 128
+# algorithmic bytes (each input read once, each output written once)
+BYTES_PER_TOKEN = H * D * 2 * 3 + H * D * 4 + H * 4 + H * D * 2   # 147,840
+STATE_BYTES = H * D * D * 4                                         # 6,291,456 per document
+DECODE_BYTES_PER_SEQ = H * (2 * D * D * 4 + 3 * D * 2 + D * 4 + 4 + D * 2)  # 96 * 132,612
+# recurrent-form flops per token and head: two column reductions + the update
+FLOPS_PER_TOKEN_HEAD = 6 * D * D
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return {"hbm_gbs": float(p["hbm_gbs"]), "bf16_tflops": float(p["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+
+
+# ------------------------------------------------------------------ distributed
+
+class Dist:
+    def __init__(self):
+        self.world = int(os.environ.get("WORLD_SIZE", "1"))
+        self.rank = int(os.environ.get("RANK", "0"))
+        self.local = int(os.environ.get("LOCAL_RANK", "0"))
+        self.pg = None
+
+    def init(self, backend):
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group(backend=backend)
+            self.pg = dist
+
+    def barrier(self):
+        if self.pg is not None:
+            self.pg.barrier()
+
+    def max(self, x: float) -> float:
+        if self.pg is None:
+            return x
+        dev = "cuda" if torch.cuda.is_available() and self.pg.get_backend() == "nccl" else "cpu"
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        self.pg.all_reduce(t, op=self.pg.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.pg is not None:
+            self.pg.destroy_process_group()
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi samples (200 ms) while GPU work runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="kda_clocks_", suffix=".csv")
+            os.close(fd)
+            self.out = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)], stdout=self.out,
+                stderr=subprocess.DEVNULL)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.out.close()
+        rows = []
+        with open(self.path) as f:
+            for line in f:
+                parts = [p.strip() for p in line.split(",")]
+                if len(parts) >= 9:
+                    rows.append(parts)
+        os.unlink(self.path)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        smax = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        loaded = [s for s in sm if smax and s > 0.5 * max(smax)] or sm
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(smax) if smax else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# ------------------------------------------------------------------ timing
+
+def time_steps(dist, step, steps, warmup, counter=None):
+    """Run `step` warmup + steps times; return (total_ms max over ranks,
+    per-step ms list from events around each step on the current stream,
+    kernels launched inside the timed region when `counter` is given)."""
+    for _ in range(warmup):
+        step()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    n0 = counter() if counter else 0
+    t0.record()
+    for a, b in ev:
+        a.record()
+        step()
+        b.record()
+    t1.record()
+    n1 = counter() if counter else 0
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    total = dist.max(t0.elapsed_time(t1))
+    per = [a.elapsed_time(b) for a, b in ev]
+    return (total, per, n1 - n0) if counter else (total, per)
+
+
+def roofline(bytes_per_launch, launch_ms, peak_gbs, traffic=None):
+    achieved = bytes_per_launch / (launch_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
+            "frac": round(achieved / peak_gbs, 4), "traffic": traffic,
+            "algorithmic_bytes": int(bytes_per_launch)}
+
+
+# ------------------------------------------------------------------ workloads
+
+def bench_prefill(kda, synth, dist, args, peaks):
+    inp = synth.inputs(2, device="cuda")
+    T = inp["q"].shape[0]
+    out = torch.empty_like(inp["v"])
+    fin = torch.empty(1, H, D, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_prefill_workspace_size(H, D, torch.bfloat16, T, 1),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None,
+                        out=out, final_state=fin, workspace=ws)
+
+    total_ms, per, launches_timed = time_steps(dist, step, args.steps, args.warmup,
+                                               counter=kda.kda_kernel_launches)
+    bytes_launch = BYTES_PER_TOKEN * T + STATE_BYTES
+    res = {"total_ms": total_ms, "tokens": T, "launch_ms": statistics.mean(per),
+           "roofline": roofline(bytes_launch, statistics.mean(per), peaks["hbm_gbs"]),
+           "gpu_launches": int(launches_timed)}
+
+    # end to end: pinned host inputs -> device, prefill, outputs -> pinned host
+    host = {k: inp[k].cpu().pin_memory() for k in ("q", "k", "v", "g", "beta")}
+    h_out = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    h_fin = torch.empty(fin.shape, dtype=fin.dtype).pin_memory()
+    dbuf = {k: torch.empty_like(inp[k]) for k in host}
+
+    def e2e_step():
+        for k_, h_ in host.items():
+            dbuf[k_].copy_(h_, non_blocking=True)
+        kda.kda_prefill(dbuf["q"], dbuf["k"], dbuf["v"], dbuf["g"], dbuf["beta"], None, None,
+                        out=out, final_state=fin, workspace=ws)
+        h_out.copy_(out, non_blocking=True)
+        h_fin.copy_(fin, non_blocking=True)
+
+    e2e_ms, _ = time_steps(dist, e2e_step, args.steps, args.warmup)
+    res["e2e"] = {"value": round(dist.world * T * args.steps / (e2e_ms * 1e-3), 1),
+                  "unit": "tokens/s",
+                  "h2d_bytes_per_step": int(sum(h.numel() * h.element_size()
+                                                for h in host.values())),
+                  "d2h_bytes_per_step": int(h_out.numel() * h_out.element_size()
+                                            + h_fin.numel() * h_fin.element_size())}
+    del inp, host, dbuf
+    return res
+
+
+def bench_decode(kda, synth, dist, args, peaks):
+    inp = synth.inputs(5, device="cuda")
+    N = inp["q"].shape[0]
+    state = inp["init_state"]
+    out = torch.empty_like(inp["v"])
+
+    def step():
+        kda.kda_decode_step(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], state, out=out)
+
+    total_ms, per = time_steps(dist, step, args.steps, args.warmup)
+    steps_s = args.steps / (total_ms * 1e-3)
+    return {"workload": "decode: 256 sequences x 1 token, H=96, d=128, fp32 state in place",
+            "value": round(steps_s * dist.world, 2), "unit": "steps/s",
+            "tokens_per_s": round(steps_s * N * dist.world, 1),
+            "ms_per_step": round(total_ms / args.steps, 4),
+            "roofline": roofline(DECODE_BYTES_PER_SEQ * N, statistics.mean(per),
+                                 peaks["hbm_gbs"])}
+
+
+def bench_long(kda, dist, args, peaks):
+    T = 262144
+    g = torch.Generator(device="cuda").manual_seed(3)
+    mk = lambda *s, dt=torch.float32: torch.randn(*s, generator=g, device="cuda",
+                                                  dtype=torch.float32).to(dt)
+    q_raw, k_raw, v_raw = (mk(T, H, D, dt=torch.bfloat16) for _ in range(3))
+    conv_w = 0.5 * mk(3, H * D, 4)
+    z_g, z_b = mk(T, H, D), mk(T, H)
+    q, k, v = (torch.empty_like(q_raw) for _ in range(3))
+    gg, bb = torch.empty_like(z_g), torch.empty_like(z_b)
+    out = torch.empty_like(q_raw)
+    fin = torch.empty(1, H, D, D, dtype=torch.float32, device="cuda")
+    ws = torch.empty(kda.kda_prefill_workspace_size(H, D, torch.bfloat16, T, 1),
+                     dtype=torch.uint8, device="cuda")
+
+    def step():
+        kda.kda_prologue(q_raw, k_raw, v_raw, conv_w, z_g, z_b, None, outs=(q, k, v, gg, bb))
+        kda.kda_prefill(q, k, v, gg, bb, None, None, out=out, final_state=fin, workspace=ws)
+
+    steps = max(1, min(args.steps, args.long_steps))
+    total_ms, per = time_steps(dist, step, steps, min(args.warmup, 3))
+    bytes_step = BYTES_PER_TOKEN * T + STATE_BYTES + conv_w.numel() * 4
+    return {"workload": "long context: T=262144, H=96, d=128, raw bf16 q/k/v through the "
+                        "fused prologue, then prefill",
+            "value": round(dist.world * T * steps / (total_ms * 1e-3), 1), "unit": "tokens/s",
+            "ms_per_step": round(total_ms / steps, 3), "steps": steps,
+            "roofline": roofline(bytes_step, statistics.mean(per), peaks["hbm_gbs"]),
+            "note": "bytes credited: raw q/k/v, z_g, z_beta in, out and final state written once"}
+
+
+def cpu_baseline(synth, heads):
+    """fp64 oracle on the host cores over `heads` of the T=4096 workload."""
+    import oracle
+    from tests.kda_testlib import oracle_prefill
+    inp = synth.inputs(2, heads=list(range(heads)))
+    T = inp["q"].shape[0]
+    t = time.perf_counter()
+    oracle_prefill(inp)
+    wall = time.perf_counter() - t
+    cores = min(heads, os.cpu_count() or 1)
+    return {"value": round(T * heads / H / wall, 2), "unit": "tokens/s", "cores": cores,
+            "kind": "oracle", "sample": f"T=4096 workload, {heads} of 96 heads, all tokens; "
+            f"tokens/s scaled to 96 heads ({wall:.2f} s wall)"}
+
+
+def base_line(args, dist, dtype):
+    return {"metric": METRIC, "unit": "tokens/s", "n_gpus": dist.world, "steps": args.steps,
+            "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": dtype, "data": "synthetic",
+            "config": {"workload": "prefill: 1 sequence, T=4096, H=96, d_k=d_v=128, bf16 "
+                                   "q/k/v, fp32 g/beta, zero initial state",
+                       "T": 4096, "H": H, "d": D, "documents": 1,
+                       "l2": "inputs 612 MB > 129 MB L2 (no flush)",
+                       "parallelism": f"replicas x{dist.world}" if dist.world > 1 else "1 GPU"}}
+
+
+def run_reference(args, dist):
+    import synth
+    if dist.rank != 0:
+        return 0
+    heads = args.ref_heads
+    cb = None
+    vals = []
+    for i in range(args.warmup + args.steps):
+        cb = cpu_baseline(synth, heads)
+        if i >= args.warmup:
+            vals.append(cb["value"])
+    value = statistics.mean(vals)
+    line = base_line(args, dist, "f64")
+    line.update({"impl": "reference", "value": round(value, 2), "n_gpus": 1,
+                 "ms_per_step": round(4096 / value * 1e3, 2),
+                 "cpu_baseline": dict(cb, value=round(value, 2)),
+                 "e2e": {"value": round(value, 2), "unit": "tokens/s",
+                         "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}})
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
+    ap.add_argument("--long-steps", type=int, default=5)
+    ap.add_argument("--ref-heads", type=int, default=16)
+    ap.add_argument("--no-long", action="store_true")
+    ap.add_argument("--no-decode", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    dist = Dist()
+    if args.impl == "reference":
+        return run_reference(args, dist)
+
+    torch.cuda.set_device(dist.local)
+    dist.init("nccl")
+    import synth
+    from linear_attention_03_gb300 import kda
+
+    peaks = load_peaks()
+    clocks = ClockSampler(dist.local)
+    clocks.start()
+    pre = bench_prefill(kda, synth, dist, args, peaks)
+    dec = None if args.no_decode else bench_decode(kda, synth, dist, args, peaks)
+    torch.cuda.empty_cache()
+    lng = None if args.no_long else bench_long(kda, dist, args, peaks)
+    clk = clocks.stop()
+    cb = None
+    if dist.rank == 0 and not args.no_cpu_baseline:
+        cb = cpu_baseline(synth, H)
+
+    if dist.rank == 0:
+        line = base_line(args, dist, "bf16")
+        line.update({
+            "value": round(dist.world * pre["tokens"] * args.steps / (pre["total_ms"] * 1e-3), 1),
+            "ms_per_step": round(pre["total_ms"] / args.steps, 4),
+            "roofline": dict(pre["roofline"], peak_source=f"{peaks['source']} HBM copy"),
+            "cpu_baseline": cb, "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"],
+            "clocks": clk, "decode": dec, "long_context": lng})
+        print(json.dumps(line), flush=True)
+    dist.close()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

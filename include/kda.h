@@ -1,0 +1,179 @@
+/*
+ * kda.h -- C ABI of the Kimi Delta Attention (KDA) operator for NVIDIA GB300
+ * (sm_103a).
+ *
+ * KDA is the gated delta-rule recurrence with one retention value per key
+ * channel.  Per head, with a state S of d_k x d_v numbers (row i = key
+ * channel i):
+ *
+ *     S_t = (I - beta_t k_t k_t^T) Diag(alpha_t) S_{t-1} + beta_t k_t v_t^T,
+ *     alpha_t = exp(g_t),     o_t = S_t^T q_t   (read after the update)
+ *
+ * Sources (page title -- section):
+ *   "Kimi K3 Architecture Explained" -- Step 3 "Forgetting, Channel by
+ *       Channel" (the recurrence, rows = key channels) and "Inside a KDA Layer".
+ *   "From GPT-2 to Kimi K3, from first principles" -- Chapter 5 (the four
+ *       verbs retain/erase/write/read; g = gmin*sigmoid(z), gmin = -5) and
+ *       Chapter 6 (chunked prefill vs. fused-recurrent single-token decode).
+ *   "An infra-oriented diagram of Kimi K3" -- KDA card (96 heads, 128 x 128
+ *       state, width-4 depthwise causal conv, Swish, L2Norm, scaled-sigmoid
+ *       decay, sigmoid beta) and the packed-token note (cumulative sequence
+ *       offsets delimit documents).
+ *
+ * Conventions shared by every entry point
+ *   - All tensor arguments are DEVICE pointers owned by the caller; the
+ *     library never allocates, frees or keeps them.  Tensors are dense,
+ *     row-major and 16-byte aligned.
+ *   - Layouts:  q, k, g   [T, H, d_k]      v, out  [T, H, d_v]
+ *               beta      [T, H]           states  [N, H, d_k, d_v] fp32
+ *               cu_seqlens [N + 1] int32: document n owns tokens
+ *               cu_seqlens[n] .. cu_seqlens[n+1]-1; cu_seqlens[0] = 0 and
+ *               cu_seqlens[N] = T.  Documents never see each other: state
+ *               and conv history restart at every document.
+ *   - q/k/v (and out) are fp32 or bf16 (kda_dims.qkv_dtype); g, beta and
+ *     every state are fp32.  Arithmetic is fp32 on CUDA cores or bf16
+ *     operands with fp32 accumulation on the tensor cores.
+ *   - Supported head sizes: d_k = d_v in {16, 32, 64, 128}; anything else
+ *     returns KDA_ERR_UNSUPPORTED.  The tensor-core prefill serves
+ *     d = 128 with bf16 inputs; the other shapes use the CUDA-core path.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Every call
+ *     is asynchronous: the returned status covers argument checks and the
+ *     kernel launches only.  Invalid arguments return an error and launch
+ *     nothing.  Errors found on the device go to the workspace status word
+ *     (kda_get_device_status).
+ *   - kda_last_error() returns a thread-local message for the last failure.
+ */
+#ifndef KDA_H
+#define KDA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define KDA_API __attribute__((visibility("default")))
+#else
+#define KDA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    KDA_OK = 0,
+    KDA_ERR_INVALID = 1,      /* bad pointer, size, alignment or layout      */
+    KDA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head size, dtype) */
+    KDA_ERR_CUDA = 3,         /* a CUDA runtime call failed                   */
+    KDA_ERR_TIMEOUT = 4,      /* a device-side wait gave up (status word)     */
+    KDA_ERR_DEVICE = 5        /* the device flagged bad input (status word)   */
+} kda_status;
+
+typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
+
+/* Device status word values (kda_get_device_status). */
+#define KDA_DEVICE_OK 0
+#define KDA_DEVICE_BAD_OFFSETS 1  /* cu_seqlens not 0..T and non-decreasing */
+#define KDA_DEVICE_TIMEOUT 2      /* a bounded device-side wait ran out      */
+
+typedef struct {
+    int32_t H;          /* heads                                   */
+    int32_t d_k;        /* key/query channels per head             */
+    int32_t d_v;        /* value channels per head (= d_k)         */
+    int32_t qkv_dtype;  /* kda_dtype of q, k, v and of out         */
+} kda_dims;
+
+/*
+ * Bytes of device workspace kda_prefill needs for T packed tokens in N
+ * documents (never 0: it always holds the device status word).  The caller
+ * allocates it, 256-byte aligned, and may reuse it across calls that do not
+ * overlap on the GPU.
+ */
+KDA_API size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N);
+
+/*
+ * Multi-token prefill of N packed documents ("chunk" mode of "From GPT-2 to
+ * Kimi K3", Chapter 6; the recurrence of "Kimi K3 Architecture Explained",
+ * Step 3).
+ *   q, k     [T, H, d_k]  qkv_dtype; q and k are expected L2-normalised
+ *   v        [T, H, d_v]  qkv_dtype
+ *   g        [T, H, d_k]  fp32 log-decay (alpha = exp(g)), normally in (-5, 0)
+ *   beta     [T, H]       fp32 write strength
+ *   init_state [N, H, d_k, d_v] fp32 or NULL (zero state)
+ *   cu_seqlens [N + 1] int32 device offsets, or NULL when N == 1 (one
+ *              document of T tokens)
+ *   out      [T, H, d_v]  qkv_dtype, written for every token
+ *   final_state [N, H, d_k, d_v] fp32 or NULL; may alias init_state
+ *   workspace  kda_prefill_workspace_size() bytes; its status word is
+ *              cleared by this call and set if the device finds cu_seqlens
+ *              invalid (then out and final_state are unspecified).
+ * g is used as given; the tensor-core path relies on g >= -5 per token (the
+ * bounded gate) to keep its 16-token rescaling factors inside fp32 range.
+ * T = 0 is allowed (final_state = init_state).
+ */
+KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v,
+                       const float *g, const float *beta,
+                       const float *init_state, const int32_t *cu_seqlens,
+                       int32_t N, int64_t T, kda_dims dims, void *out,
+                       float *final_state, void *workspace,
+                       size_t workspace_bytes, void *stream);
+
+/*
+ * One decode step for N independent sequences, one token each
+ * ("fused_recurrent" mode of "From GPT-2 to Kimi K3", Chapter 6).  Reads
+ * every fp32 state once and writes it back in place.
+ *   q, k [N, H, d_k]; v, out [N, H, d_v]  qkv_dtype
+ *   g    [N, H, d_k] fp32;  beta [N, H] fp32
+ *   state [N, H, d_k, d_v] fp32, updated in place
+ * Equivalent to kda_prefill with N one-token documents.
+ */
+KDA_API kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, float *state,
+                           void *out, int32_t N, kda_dims dims, void *stream);
+
+/*
+ * The KDA input path of the infra diagram's KDA card, fused into one pass
+ * per tensor:
+ *   q, k, v = Swish(ShortConv_4(raw))   (depthwise, causal, no bias, zero
+ *                                        history at each document start;
+ *                                        tap 3 multiplies the current token)
+ *   q, k   /= sqrt(sum over the head's d channels of x^2 + 1e-6)
+ *   g      = -5 * sigmoid(z_g)          ("From GPT-2 to Kimi K3", Chapter 5)
+ *   beta   = sigmoid(z_beta)
+ *   q_raw, k_raw, v_raw [T, H, d] qkv_dtype;  conv_w [3, H*d, 4] fp32
+ *   (filters of q, k, v; channel h*d + c);  z_g [T, H, d] fp32 or NULL;
+ *   z_beta [T, H] fp32 or NULL (the matching output is then not written);
+ *   cu_seqlens [N + 1] int32 device offsets or NULL when N == 1.
+ *   Outputs q, k, v [T, H, d] qkv_dtype; g [T, H, d] fp32; beta [T, H] fp32.
+ * Offsets are clamped to [0, T] on the device, so bad offsets cannot cause
+ * out-of-range accesses; the results are then unspecified.
+ */
+KDA_API kda_status kda_prologue(const void *q_raw, const void *k_raw,
+                        const void *v_raw, const float *conv_w,
+                        const float *z_g, const float *z_beta,
+                        const int32_t *cu_seqlens, int32_t N, int64_t T,
+                        kda_dims dims, void *q, void *k, void *v, float *g,
+                        float *beta, void *stream);
+
+/*
+ * Waits for `stream`, then copies the workspace status word (one of the
+ * KDA_DEVICE_* values) to *status_out.  Returns KDA_ERR_DEVICE /
+ * KDA_ERR_TIMEOUT when the word is set, KDA_OK when it is clear.
+ */
+KDA_API kda_status kda_get_device_status(const void *workspace, int32_t *status_out,
+                                 void *stream);
+
+/* Thread-local text of the last error of this thread ("" if none). */
+KDA_API const char *kda_last_error(void);
+
+/*
+ * Number of CUDA kernels this library has queued in this process since it
+ * was loaded (all threads, all devices).  Runtime memsets/copies are not
+ * counted.  Lets a caller check how many kernels a timed region launched.
+ */
+KDA_API uint64_t kda_kernel_launches(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H */

@@ -1,0 +1,188 @@
+// kda_api.cu -- the C ABI declared in include/kda.h: argument checks,
+// path selection and kernel launches.  No allocation happens here; every
+// buffer belongs to the caller.
+#include <stdio.h>
+#include <string.h>
+
+#include <atomic>
+
+#include "kda_internal.cuh"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+std::atomic<uint64_t> g_launches{0};
+
+kda_status fail(kda_status code, const char *fmt, const char *what = "") {
+    snprintf(g_last_error, sizeof(g_last_error), fmt, what);
+    return code;
+}
+
+kda_status cuda_fail(cudaError_t err, const char *where) {
+    snprintf(g_last_error, sizeof(g_last_error), "%s: %s", where, cudaGetErrorString(err));
+    return KDA_ERR_CUDA;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+kda_status check_dims(const kda_dims &d) {
+    if (d.H < 1) return fail(KDA_ERR_INVALID, "H must be >= 1%s");
+    if (d.qkv_dtype != KDA_F32 && d.qkv_dtype != KDA_BF16)
+        return fail(KDA_ERR_UNSUPPORTED, "qkv_dtype must be KDA_F32 or KDA_BF16%s");
+    if (d.d_k != d.d_v)
+        return fail(KDA_ERR_UNSUPPORTED, "d_k must equal d_v%s");
+    if (d.d_k != 16 && d.d_k != 32 && d.d_k != 64 && d.d_k != 128)
+        return fail(KDA_ERR_UNSUPPORTED, "head size must be 16, 32, 64 or 128%s");
+    return KDA_OK;
+}
+
+// required pointer: non-null and 16-byte aligned; optional: null or aligned
+kda_status need(const void *p, const char *name) {
+    if (p == nullptr) return fail(KDA_ERR_INVALID, "%s must not be NULL", name);
+    if (!aligned16(p)) return fail(KDA_ERR_INVALID, "%s must be 16-byte aligned", name);
+    return KDA_OK;
+}
+
+kda_status maybe(const void *p, const char *name) {
+    if (p != nullptr && !aligned16(p))
+        return fail(KDA_ERR_INVALID, "%s must be 16-byte aligned", name);
+    return KDA_OK;
+}
+
+#define KDA_TRY(expr)                        \
+    do {                                     \
+        const kda_status _s = (expr);        \
+        if (_s != KDA_OK) return _s;         \
+    } while (0)
+
+constexpr size_t kStatusBytes = 256;
+
+}  // namespace
+
+void kda::count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+extern "C" {
+
+const char *kda_last_error(void) { return g_last_error; }
+
+uint64_t kda_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N) {
+    (void)dims;
+    (void)T;
+    (void)N;
+    return kStatusBytes;
+}
+
+kda_status kda_prefill(const void *q, const void *k, const void *v,
+                       const float *g, const float *beta,
+                       const float *init_state, const int32_t *cu_seqlens,
+                       int32_t N, int64_t T, kda_dims dims, void *out,
+                       float *final_state, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (N < 1 || N > 65535) return fail(KDA_ERR_INVALID, "N must be in [1, 65535]%s");
+    if (T < 0 || T > INT32_MAX) return fail(KDA_ERR_INVALID, "T must be in [0, 2^31)%s");
+    if (cu_seqlens == nullptr && N != 1)
+        return fail(KDA_ERR_INVALID, "cu_seqlens may be NULL only when N == 1%s");
+    if (T > 0) {
+        KDA_TRY(need(q, "q"));
+        KDA_TRY(need(k, "k"));
+        KDA_TRY(need(v, "v"));
+        KDA_TRY(need(g, "g"));
+        KDA_TRY(need(beta, "beta"));
+        KDA_TRY(need(out, "out"));
+    }
+    KDA_TRY(maybe(init_state, "init_state"));
+    KDA_TRY(maybe(final_state, "final_state"));
+    KDA_TRY(maybe(cu_seqlens, "cu_seqlens"));
+    KDA_TRY(need(workspace, "workspace"));
+    if (workspace_bytes < kda_prefill_workspace_size(dims, T, N))
+        return fail(KDA_ERR_INVALID, "workspace too small (see kda_prefill_workspace_size)%s");
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t *status = static_cast<int32_t *>(workspace);
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    if (err != cudaSuccess) return cuda_fail(err, "clearing the status word");
+    err = kda::launch_prefill_recurrent(q, k, v, g, beta, init_state, cu_seqlens, N, T,
+                                        dims.H, dims.d_k, (kda_dtype)dims.qkv_dtype, out,
+                                        final_state, status, s);
+    if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
+    return KDA_OK;
+}
+
+kda_status kda_decode_step(const void *q, const void *k, const void *v,
+                           const float *g, const float *beta, float *state,
+                           void *out, int32_t N, kda_dims dims, void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (N < 0) return fail(KDA_ERR_INVALID, "N must be >= 0%s");
+    if ((int64_t)N * dims.H > INT32_MAX) return fail(KDA_ERR_INVALID, "N * H too large%s");
+    if (N == 0) return KDA_OK;
+    KDA_TRY(need(q, "q"));
+    KDA_TRY(need(k, "k"));
+    KDA_TRY(need(v, "v"));
+    KDA_TRY(need(g, "g"));
+    KDA_TRY(need(beta, "beta"));
+    KDA_TRY(need(state, "state"));
+    KDA_TRY(need(out, "out"));
+    cudaError_t err = kda::launch_decode(q, k, v, g, beta, state, out, N, dims.H, dims.d_k,
+                                         (kda_dtype)dims.qkv_dtype,
+                                         static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "decode launch");
+    return KDA_OK;
+}
+
+kda_status kda_prologue(const void *q_raw, const void *k_raw,
+                        const void *v_raw, const float *conv_w,
+                        const float *z_g, const float *z_beta,
+                        const int32_t *cu_seqlens, int32_t N, int64_t T,
+                        kda_dims dims, void *q, void *k, void *v, float *g,
+                        float *beta, void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (N < 1) return fail(KDA_ERR_INVALID, "N must be >= 1%s");
+    if (T < 0 || T > INT32_MAX) return fail(KDA_ERR_INVALID, "T must be in [0, 2^31)%s");
+    if (cu_seqlens == nullptr && N != 1)
+        return fail(KDA_ERR_INVALID, "cu_seqlens may be NULL only when N == 1%s");
+    if (T == 0) return KDA_OK;
+    KDA_TRY(need(q_raw, "q_raw"));
+    KDA_TRY(need(k_raw, "k_raw"));
+    KDA_TRY(need(v_raw, "v_raw"));
+    KDA_TRY(need(conv_w, "conv_w"));
+    KDA_TRY(need(q, "q"));
+    KDA_TRY(need(k, "k"));
+    KDA_TRY(need(v, "v"));
+    KDA_TRY(maybe(z_g, "z_g"));
+    KDA_TRY(maybe(z_beta, "z_beta"));
+    KDA_TRY(maybe(cu_seqlens, "cu_seqlens"));
+    if (z_g != nullptr) KDA_TRY(need(g, "g"));
+    if (z_beta != nullptr && beta == nullptr)
+        return fail(KDA_ERR_INVALID, "beta must not be NULL when z_beta is given%s");
+    cudaError_t err = kda::launch_prologue(q_raw, k_raw, v_raw, conv_w, z_g, z_beta,
+                                           cu_seqlens, N, T, dims.H, dims.d_k,
+                                           (kda_dtype)dims.qkv_dtype, q, k, v, g, beta,
+                                           static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "prologue launch");
+    return KDA_OK;
+}
+
+kda_status kda_get_device_status(const void *workspace, int32_t *status_out,
+                                 void *stream) {
+    g_last_error[0] = '\0';
+    if (workspace == nullptr || status_out == nullptr)
+        return fail(KDA_ERR_INVALID, "workspace and status_out must not be NULL%s");
+    int32_t word = 0;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t err = cudaMemcpyAsync(&word, workspace, sizeof(word), cudaMemcpyDeviceToHost, s);
+    if (err == cudaSuccess) err = cudaStreamSynchronize(s);
+    if (err != cudaSuccess) return cuda_fail(err, "reading the status word");
+    *status_out = word;
+    if (word == KDA_DEVICE_OK) return KDA_OK;
+    if (word == KDA_DEVICE_TIMEOUT)
+        return fail(KDA_ERR_TIMEOUT, "a device-side wait gave up%s");
+    return fail(KDA_ERR_DEVICE, "the device rejected cu_seqlens (not 0..T, non-decreasing)%s");
+}
+
+}  // extern "C"

@@ -1,0 +1,109 @@
+// kda_internal.cuh -- helpers shared by the KDA kernels and their launchers.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "kda.h"
+
+namespace kda {
+
+// ------------------------------------------------------------ element access
+
+template <typename T> struct Elem;
+
+template <> struct Elem<float> {
+    static __device__ __forceinline__ float load(const float *p) { return *p; }
+    static __device__ __forceinline__ void store(float *p, float x) { *p = x; }
+    // 8 consecutive elements (32 bytes, two 16-byte loads)
+    static __device__ __forceinline__ void load8(const float *p, float (&x)[8]) {
+        const float4 a = __ldg(reinterpret_cast<const float4 *>(p));
+        const float4 b = __ldg(reinterpret_cast<const float4 *>(p) + 1);
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+    static __device__ __forceinline__ void store8(float *p, const float (&x)[8]) {
+        reinterpret_cast<float4 *>(p)[0] = make_float4(x[0], x[1], x[2], x[3]);
+        reinterpret_cast<float4 *>(p)[1] = make_float4(x[4], x[5], x[6], x[7]);
+    }
+};
+
+template <> struct Elem<__nv_bfloat16> {
+    static __device__ __forceinline__ float load(const __nv_bfloat16 *p) {
+        return __bfloat162float(*p);
+    }
+    static __device__ __forceinline__ void store(__nv_bfloat16 *p, float x) {
+        *p = __float2bfloat16_rn(x);
+    }
+    static __device__ __forceinline__ void load8(const __nv_bfloat16 *p, float (&x)[8]) {
+        const uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            // bf16 -> fp32 is a 16-bit shift
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+    static __device__ __forceinline__ void store8(__nv_bfloat16 *p, const float (&x)[8]) {
+        uint32_t w[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            __nv_bfloat162 h = __floats2bfloat162_rn(x[2 * i], x[2 * i + 1]);
+            w[i] = *reinterpret_cast<uint32_t *>(&h);
+        }
+        *reinterpret_cast<uint4 *>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+};
+
+// Offsets of document n, or false when they are out of order / out of range.
+__device__ __forceinline__ bool doc_bounds(const int32_t *cu_seqlens, int32_t n,
+                                           int32_t N, int64_t T, int64_t &bos,
+                                           int64_t &eos) {
+    if (cu_seqlens == nullptr) {
+        bos = 0;
+        eos = T;
+        return true;
+    }
+    bos = cu_seqlens[n];
+    eos = cu_seqlens[n + 1];
+    if (bos < 0 || eos < bos || eos > T) return false;
+    if (n == 0 && bos != 0) return false;
+    if (n == N - 1 && eos != T) return false;
+    return true;
+}
+
+__device__ __forceinline__ void flag_status(int32_t *status, int32_t code) {
+    if (status != nullptr) atomicCAS(status, KDA_DEVICE_OK, code);
+}
+
+// Count of kernels queued by this library (kda_kernel_launches).
+void count_launches(uint64_t n);
+
+// ------------------------------------------------------------ launchers
+// Each returns the launch error (cudaSuccess when the kernels were queued).
+
+cudaError_t launch_decode(const void *q, const void *k, const void *v,
+                          const float *g, const float *beta, float *state,
+                          void *out, int32_t N, int32_t H, int32_t D,
+                          kda_dtype dt, cudaStream_t stream);
+
+cudaError_t launch_prologue(const void *q_raw, const void *k_raw,
+                            const void *v_raw, const float *conv_w,
+                            const float *z_g, const float *z_beta,
+                            const int32_t *cu_seqlens, int32_t N, int64_t T,
+                            int32_t H, int32_t D, kda_dtype dt, void *q,
+                            void *k, void *v, float *g, float *beta,
+                            cudaStream_t stream);
+
+cudaError_t launch_prefill_recurrent(const void *q, const void *k,
+                                     const void *v, const float *g,
+                                     const float *beta, const float *init_state,
+                                     const int32_t *cu_seqlens, int32_t N,
+                                     int64_t T, int32_t H, int32_t D,
+                                     kda_dtype dt, void *out,
+                                     float *final_state, int32_t *status,
+                                     cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,220 @@
+// kda_prologue.cu -- the KDA input path of "An infra-oriented diagram of
+// Kimi K3" (KDA card: "q, k, v ... ShortConv, Swish; q and k then L2Norm";
+// "scaled sigmoid bounds log-decay to (-5, 0)"; "beta ... followed by
+// sigmoid"), and the lower-bounded decay of "From GPT-2 to Kimi K3, from
+// first principles", Chapter 5 (g = gmin * sigmoid(z), gmin = -5).
+//
+// Kernel 1 (conv_swish_norm): one pass over a raw q, k or v tensor.  Each
+// thread owns 8 consecutive channels of one head (16-byte loads for bf16) and
+// walks a tile of TT tokens, keeping the last three raw inputs of its
+// channels in registers as the causal window:
+//     y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t     (fp32)
+// History is zero before each document start (cu_seqlens).  Then
+// s = y * sigmoid(y); for q and k the head's d channels are scaled by
+// 1 / sqrt(sum s^2 + 1e-6), the sum taken with shuffles among the d/8 lanes
+// that own the head.  HBM-bound: every raw element is read once (plus a
+// three-token halo per tile) and every output written once.
+//
+// Kernel 2 (gates): elementwise g = -5 sigmoid(z_g), beta = sigmoid(z_beta).
+#include "kda_internal.cuh"
+
+namespace kda {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kTileTokens = 32;   // tokens per CTA
+constexpr int kBatch = 8;         // tokens loaded ahead per thread
+constexpr float kL2Eps = 1e-6f;
+constexpr float kGmin = -5.0f;
+
+// index of the document holding token t (largest n with cu[n] <= t), with
+// every offset clamped into [0, T] so bad offsets stay in bounds
+__device__ __forceinline__ int find_doc(const int32_t *cu, int N, int64_t T, int64_t t) {
+    int lo = 0, hi = N - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        const int64_t c = min((int64_t)max(cu[mid], 0), T);
+        if (c <= t) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
+__device__ __forceinline__ int64_t clamp_off(const int32_t *cu, int n, int N, int64_t T) {
+    if (cu == nullptr) return n == 0 ? 0 : T;
+    if (n > N) return T;
+    return min((int64_t)max(cu[n], 0), T);
+}
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(kThreads)
+conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
+                       const Tin *__restrict__ x2, const float *__restrict__ conv_w,
+                       const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
+                       Tin *__restrict__ y0, Tin *__restrict__ y1, Tin *__restrict__ y2) {
+    constexpr int TPH = D / 8;                     // lanes per head
+    constexpr int HPB = kThreads / TPH;            // heads per CTA
+    const int which = blockIdx.z;                  // 0 = q, 1 = k, 2 = v
+    const Tin *x = which == 0 ? x0 : (which == 1 ? x1 : x2);
+    Tin *y = which == 0 ? y0 : (which == 1 ? y1 : y2);
+    const bool normalise = which < 2;
+
+    const int h = blockIdx.y * HPB + threadIdx.x / TPH;
+    const int sub = threadIdx.x % TPH;
+    const bool live = h < H;
+    const int64_t row_stride = (int64_t)H * D;
+    const int64_t ch = (int64_t)(live ? h : 0) * D + 8 * sub;   // first channel
+
+    float w[4][8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e)
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            w[j][e] = live ? conv_w[((int64_t)which * row_stride + ch + e) * 4 + j] : 0.f;
+
+    const int64_t t0 = (int64_t)blockIdx.x * kTileTokens;
+    const int64_t t1 = min(T, t0 + kTileTokens);
+    int n = cu ? find_doc(cu, N, T, t0) : 0;
+    int64_t start = clamp_off(cu, n, N, T);
+    int64_t next = clamp_off(cu, n + 1, N, T);
+
+    float hist[3][8];                              // x_{t-3}, x_{t-2}, x_{t-1}
+#pragma unroll
+    for (int j = 0; j < 3; ++j) {
+        const int64_t tj = t0 - 3 + j;
+        if (live && tj >= start && tj >= 0) {
+            Elem<Tin>::load8(x + tj * row_stride + ch, hist[j]);
+        } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
+        }
+    }
+
+    for (int64_t tb = t0; tb < t1; tb += kBatch) {
+        float cur[kBatch][8];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            if (live && tb + b < t1) {
+                Elem<Tin>::load8(x + (tb + b) * row_stride + ch, cur[b]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) cur[b][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const int64_t t = tb + b;
+            if (t >= t1) break;                     // uniform across the CTA
+            while (t >= next && n < N - 1) {        // entered a new document
+                ++n;
+                start = clamp_off(cu, n, N, T);
+                next = clamp_off(cu, n + 1, N, T);
+#pragma unroll
+                for (int j = 0; j < 3; ++j)
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
+            }
+            float s[8];
+            float ss = 0.f;
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+                const float yv = w[0][e] * hist[0][e] + w[1][e] * hist[1][e] +
+                                 w[2][e] * hist[2][e] + w[3][e] * cur[b][e];
+                s[e] = yv / (1.f + __expf(-yv));
+                ss += s[e] * s[e];
+                hist[0][e] = hist[1][e];
+                hist[1][e] = hist[2][e];
+                hist[2][e] = cur[b][e];
+            }
+            if (normalise) {
+#pragma unroll
+                for (int o = TPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+                const float inv = rsqrtf(ss + kL2Eps);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) s[e] *= inv;
+            }
+            if (live) Elem<Tin>::store8(y + t * row_stride + ch, s);
+        }
+    }
+}
+
+__global__ void gates_kernel(const float *__restrict__ z_g, const float *__restrict__ z_beta,
+                             float *__restrict__ g, float *__restrict__ beta,
+                             int64_t n_g4, int64_t n_b) {
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_g4; i += stride) {
+        float4 z = __ldcs(reinterpret_cast<const float4 *>(z_g) + i);
+        z.x = kGmin / (1.f + __expf(-z.x));
+        z.y = kGmin / (1.f + __expf(-z.y));
+        z.z = kGmin / (1.f + __expf(-z.z));
+        z.w = kGmin / (1.f + __expf(-z.w));
+        __stcs(reinterpret_cast<float4 *>(g) + i, z);
+    }
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_b; i += stride)
+        beta[i] = 1.f / (1.f + __expf(-z_beta[i]));
+}
+
+template <typename Tin, int D>
+cudaError_t run_conv(const void *q_raw, const void *k_raw, const void *v_raw,
+                     const float *conv_w, const int32_t *cu, int32_t N, int64_t T,
+                     int32_t H, void *q, void *k, void *v, cudaStream_t stream) {
+    constexpr int HPB = kThreads / (D / 8);
+    const dim3 grid((unsigned)((T + kTileTokens - 1) / kTileTokens),
+                    (unsigned)((H + HPB - 1) / HPB), 3);
+    conv_swish_norm_kernel<Tin, D><<<grid, kThreads, 0, stream>>>(
+        static_cast<const Tin *>(q_raw), static_cast<const Tin *>(k_raw),
+        static_cast<const Tin *>(v_raw), conv_w, cu, N, T, H, static_cast<Tin *>(q),
+        static_cast<Tin *>(k), static_cast<Tin *>(v));
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename Tin>
+cudaError_t run_conv_d(const void *q_raw, const void *k_raw, const void *v_raw,
+                       const float *conv_w, const int32_t *cu, int32_t N, int64_t T,
+                       int32_t H, int32_t D, void *q, void *k, void *v,
+                       cudaStream_t stream) {
+    switch (D) {
+    case 16: return run_conv<Tin, 16>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
+    case 32: return run_conv<Tin, 32>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
+    case 64: return run_conv<Tin, 64>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
+    case 128: return run_conv<Tin, 128>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_prologue(const void *q_raw, const void *k_raw,
+                            const void *v_raw, const float *conv_w,
+                            const float *z_g, const float *z_beta,
+                            const int32_t *cu_seqlens, int32_t N, int64_t T,
+                            int32_t H, int32_t D, kda_dtype dt, void *q,
+                            void *k, void *v, float *g, float *beta,
+                            cudaStream_t stream) {
+    cudaError_t err = cudaSuccess;
+    if (T > 0) {
+        err = dt == KDA_BF16
+                  ? run_conv_d<__nv_bfloat16>(q_raw, k_raw, v_raw, conv_w, cu_seqlens,
+                                              N, T, H, D, q, k, v, stream)
+                  : run_conv_d<float>(q_raw, k_raw, v_raw, conv_w, cu_seqlens, N, T,
+                                      H, D, q, k, v, stream);
+        if (err != cudaSuccess) return err;
+    }
+    const int64_t n_g4 = z_g ? T * H * D / 4 : 0;
+    const int64_t n_b = z_beta ? T * H : 0;
+    if (n_g4 + n_b > 0) {
+        int dev = 0, sms = 0;
+        cudaGetDevice(&dev);
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        const int64_t most = n_g4 > n_b ? n_g4 : n_b;
+        int64_t blocks = (most + 255) / 256;
+        if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
+        if (blocks < 1) blocks = 1;
+        gates_kernel<<<(unsigned)blocks, 256, 0, stream>>>(z_g, z_beta, g, beta, n_g4, n_b);
+        count_launches(1);
+        err = cudaGetLastError();
+    }
+    return err;
+}
+
+}  // namespace kda

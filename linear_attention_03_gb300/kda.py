@@ -1,0 +1,205 @@
+"""Python binding of libkda.so (include/kda.h): argument marshalling only.
+
+Every step of the operator runs in the CUDA library; this module checks
+tensor shapes, allocates outputs with torch when the caller gives none, and
+passes raw device pointers and the current torch stream through ctypes.
+Importing it raises if the library has not been built -- there is no
+fallback implementation.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libkda.so")
+
+if not os.path.exists(_LIB_PATH):
+    raise ImportError(f"{_LIB_PATH} is missing: build it with "
+                      "`python -m linear_attention_03_gb300.build` (needs nvcc)")
+
+lib = ctypes.CDLL(_LIB_PATH)
+
+KDA_OK, KDA_ERR_INVALID, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
+    KDA_ERR_DEVICE = range(6)
+KDA_F32, KDA_BF16 = 0, 1
+KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT = 0, 1, 2
+SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
+           "kda_prologue", "kda_get_device_status", "kda_last_error",
+           "kda_kernel_launches")
+
+
+class kda_dims(ctypes.Structure):
+    _fields_ = [("H", ctypes.c_int32), ("d_k", ctypes.c_int32),
+                ("d_v", ctypes.c_int32), ("qkv_dtype", ctypes.c_int32)]
+
+
+_P, _i32, _i64, _sz = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t
+lib.kda_prefill_workspace_size.argtypes = [kda_dims, _i64, _i32]
+lib.kda_prefill_workspace_size.restype = _sz
+lib.kda_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
+                            _sz, _P]
+lib.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
+lib.kda_prologue.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
+                             _P, _P, _P]
+lib.kda_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+lib.kda_last_error.argtypes = []
+lib.kda_last_error.restype = ctypes.c_char_p
+lib.kda_kernel_launches.argtypes = []
+lib.kda_kernel_launches.restype = ctypes.c_uint64
+for _fn in (lib.kda_prefill, lib.kda_decode_step, lib.kda_prologue, lib.kda_get_device_status):
+    _fn.restype = ctypes.c_int
+
+
+class KDAError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where} failed with status {status}: "
+                         f"{lib.kda_last_error().decode(errors='replace')}")
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return KDA_BF16
+    if t.dtype == torch.float32:
+        return KDA_F32
+    raise TypeError(f"q/k/v must be bfloat16 or float32, got {t.dtype}")
+
+
+def _dev(t, name, dtype=None, shape=None):
+    if t is None:
+        return None
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if shape is not None and tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} must have shape {tuple(shape)}, got {tuple(t.shape)}")
+    return t
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _offsets(cu_seqlens, T, device):
+    if cu_seqlens is None:
+        return None, 1
+    if isinstance(cu_seqlens, torch.Tensor) and cu_seqlens.is_cuda:
+        cu = _dev(cu_seqlens, "cu_seqlens", torch.int32)
+    else:
+        cu = torch.as_tensor(cu_seqlens, dtype=torch.int32).to(device)
+    return cu, cu.numel() - 1
+
+
+def dims_of(q: torch.Tensor) -> kda_dims:
+    _, H, d = q.shape
+    return kda_dims(H, d, d, _dtype_code(q))
+
+
+def kda_prefill_workspace_size(H: int, d: int, dtype: torch.dtype, T: int, N: int) -> int:
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib.kda_prefill_workspace_size(kda_dims(H, d, d, code), T, N))
+
+
+def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
+                final_state=None, workspace=None, want_final_state=True):
+    """Chunked prefill over packed documents; returns (out, final_state)."""
+    T, H, d = q.shape
+    dev = q.device
+    _dev(q, "q")
+    _dev(k, "k", q.dtype, q.shape)
+    _dev(v, "v", q.dtype, q.shape)
+    _dev(g, "g", torch.float32, q.shape)
+    _dev(beta, "beta", torch.float32, (T, H))
+    cu, N = _offsets(cu_seqlens, T, dev)
+    _dev(init_state, "init_state", torch.float32, (N, H, d, d))
+    if out is None:
+        out = torch.empty_like(v)
+    _dev(out, "out", q.dtype, q.shape)
+    if final_state is None and want_final_state:
+        final_state = torch.empty((N, H, d, d), dtype=torch.float32, device=dev)
+    _dev(final_state, "final_state", torch.float32, (N, H, d, d))
+    dims = dims_of(q)
+    ws_bytes = int(lib.kda_prefill_workspace_size(dims, T, N))
+    if workspace is None:
+        workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    _dev(workspace, "workspace", torch.uint8)
+    st = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                         _ptr(cu), N, T, dims, _ptr(out), _ptr(final_state),
+                         _ptr(workspace), workspace.numel(), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill")
+    return out, final_state
+
+
+def kda_decode_step(q, k, v, g, beta, state, out=None):
+    """One token per sequence; updates `state` in place and returns out."""
+    N, H, d = q.shape
+    _dev(q, "q")
+    _dev(k, "k", q.dtype, q.shape)
+    _dev(v, "v", q.dtype, q.shape)
+    _dev(g, "g", torch.float32, q.shape)
+    _dev(beta, "beta", torch.float32, (N, H))
+    _dev(state, "state", torch.float32, (N, H, d, d))
+    if out is None:
+        out = torch.empty_like(v)
+    _dev(out, "out", q.dtype, q.shape)
+    st = lib.kda_decode_step(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state),
+                             _ptr(out), N, dims_of(q), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_step")
+    return out
+
+
+def kda_prologue(q_raw, k_raw, v_raw, conv_w, z_g=None, z_beta=None, cu_seqlens=None,
+                 outs=None):
+    """Fused ShortConv + Swish + L2Norm(q, k) and the two gates.
+
+    Returns (q, k, v, g, beta); g / beta are None when their logits are None.
+    """
+    T, H, d = q_raw.shape
+    dev = q_raw.device
+    _dev(q_raw, "q_raw")
+    _dev(k_raw, "k_raw", q_raw.dtype, q_raw.shape)
+    _dev(v_raw, "v_raw", q_raw.dtype, q_raw.shape)
+    _dev(conv_w, "conv_w", torch.float32, (3, H * d, 4))
+    _dev(z_g, "z_g", torch.float32, q_raw.shape)
+    _dev(z_beta, "z_beta", torch.float32, (T, H))
+    cu, N = _offsets(cu_seqlens, T, dev)
+    if outs is None:
+        outs = (torch.empty_like(q_raw), torch.empty_like(q_raw), torch.empty_like(q_raw),
+                None if z_g is None else torch.empty_like(z_g),
+                None if z_beta is None else torch.empty_like(z_beta))
+    q, k, v, g, beta = outs
+    st = lib.kda_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w), _ptr(z_g),
+                          _ptr(z_beta), _ptr(cu), N, T, dims_of(q_raw), _ptr(q), _ptr(k),
+                          _ptr(v), _ptr(g), _ptr(beta), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prologue")
+    return q, k, v, g, beta
+
+
+def kda_get_device_status(workspace) -> int:
+    """Wait for the current stream and return the workspace status word."""
+    word = ctypes.c_int32(0)
+    st = lib.kda_get_device_status(_ptr(workspace), ctypes.byref(word), _stream())
+    if st not in (KDA_OK, KDA_ERR_DEVICE, KDA_ERR_TIMEOUT):
+        raise KDAError(st, "kda_get_device_status")
+    return int(word.value)
+
+
+def kda_last_error() -> str:
+    return lib.kda_last_error().decode(errors="replace")
+
+
+def kda_kernel_launches() -> int:
+    """Kernels this library has queued in this process so far."""
+    return int(lib.kda_kernel_launches())

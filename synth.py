@@ -122,32 +122,45 @@ def _pool():
     return _POOL
 
 
-def _heads_tensor(H, heads, draw, dtype):
-    """Torch CPU tensor [rows..., len(heads), cols]; head slot i holds draw(heads[i]).
+def _heads_tensor(H, heads, draw, dtype, device=None):
+    """Tensor [rows..., len(heads), cols]; head slot i holds draw(heads[i]).
 
     draw(h) returns a numpy array [rows..., cols] for head h.  Heads are drawn
-    on a thread pool (numpy releases the GIL while it fills arrays).
+    on a thread pool (numpy releases the GIL while it fills arrays).  With a
+    CUDA `device` the result is allocated there and filled head by head, so
+    host memory holds only a pool's worth of heads at a time.
     """
     heads = list(range(H)) if heads is None else list(heads)
     first = torch.from_numpy(np.ascontiguousarray(draw(heads[0]))).to(dtype)
     out = torch.empty(tuple(first.shape[:-1]) + (len(heads), first.shape[-1]),
-                      dtype=dtype)
+                      dtype=dtype, device=device)
     out.select(-2, 0).copy_(first)
+    rest = list(enumerate(heads))[1:]
 
     def one(ix_h):
         ix, h = ix_h
-        out.select(-2, ix).copy_(
-            torch.from_numpy(np.ascontiguousarray(draw(h))).to(dtype))
+        a = torch.from_numpy(np.ascontiguousarray(draw(h))).to(dtype)
+        if device is None:
+            out.select(-2, ix).copy_(a)
+            return None
+        return ix, a
 
-    list(_pool().map(one, list(enumerate(heads))[1:]))
+    if device is None:
+        list(_pool().map(one, rest))
+    else:
+        step = _pool()._max_workers
+        for b in range(0, len(rest), step):
+            for ix, a in _pool().map(one, rest[b:b + step]):
+                out.select(-2, ix).copy_(a)
     return out
 
 
-def inputs(index: int, heads=None) -> dict:
+def inputs(index: int, heads=None, device=None) -> dict:
     """Inputs of workload `index` as torch CPU tensors.
 
     heads: optional list of head indices; the result then holds only those
     heads, bit-identical to the same heads of the full draw.
+    device: None for CPU tensors, or a CUDA device to fill directly.
     Keys: q,k,v [T,H,d]; g [T,H,d] fp32; beta [T,H] fp32; init_state
     [N,H,d,d] fp32 or None; cu_seqlens int64 numpy [N+1];
     raw workloads give q_raw,k_raw,v_raw, conv_w [3,Hs*d,4], z_g, z_beta.
@@ -159,31 +172,31 @@ def inputs(index: int, heads=None) -> dict:
     if w.raw:
         for name, sid in (("q_raw", Q), ("k_raw", K), ("v_raw", V)):
             res[name] = _heads_tensor(H, hs, lambda h, sid=sid:
-                                      _normal(s, sid, h, (T, d)), w.dtype)
+                                      _normal(s, sid, h, (T, d)), w.dtype, device)
         res["z_g"] = _heads_tensor(H, hs, lambda h: _normal(s, ZG, h, (T, d)),
-                                   torch.float32)
+                                   torch.float32, device)
         res["z_beta"] = _heads_tensor(H, hs, lambda h: _normal(s, ZB, h, (T, 1)),
-                                      torch.float32)[..., 0]
+                                      torch.float32, device)[..., 0]
         conv = torch.stack([
             _heads_tensor(H, hs, lambda h, i=i:
-                          (0.5 * _normal(s, CONV * 16 + i, h, (4, d))), torch.float32)
+                          (0.5 * _normal(s, CONV * 16 + i, h, (4, d))), torch.float32, device)
             for i in range(3)])                       # [3, 4, Hs, d]
         res["conv_w"] = conv.permute(0, 2, 3, 1).reshape(3, len(hs) * d, 4).contiguous()
         res["init_state"] = None
         return res
     res["q"] = _heads_tensor(H, hs, lambda h: _unit(_normal(s, Q, h, (T, d))),
-                             w.dtype)
+                             w.dtype, device)
     res["k"] = _heads_tensor(H, hs, lambda h: _unit(_normal(s, K, h, (T, d))),
-                             w.dtype)
-    res["v"] = _heads_tensor(H, hs, lambda h: _normal(s, V, h, (T, d)), w.dtype)
+                             w.dtype, device)
+    res["v"] = _heads_tensor(H, hs, lambda h: _normal(s, V, h, (T, d)), w.dtype, device)
     res["g"] = _heads_tensor(H, hs, lambda h: _log_decay(_normal(s, ZG, h, (T, d))),
-                             torch.float32)
+                             torch.float32, device)
     res["beta"] = _heads_tensor(H, hs, lambda h: _logistic(_normal(s, ZB, h, (T, 1))),
-                                torch.float32)[..., 0].contiguous()
+                                torch.float32, device)[..., 0].contiguous()
     N = len(w.lengths)
     if w.init_std > 0:
         st = _heads_tensor(H, hs, lambda h: (w.init_std * _normal(
-            s, S0, h, (N, d * d))), torch.float32)        # [N, Hs, d*d]
+            s, S0, h, (N, d * d))), torch.float32, device)        # [N, Hs, d*d]
         res["init_state"] = st.reshape(N, len(hs), d, d).contiguous()
     else:
         res["init_state"] = None

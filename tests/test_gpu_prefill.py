@@ -1,0 +1,97 @@
+"""GPU prefill vs the fp64 oracle: element by element on small and ragged
+shapes that span several 64-token chunks with a ragged tail, packed
+documents (including empty and one-token ones), every supported head size
+and dtype, and the structural invariants (split runs, aliasing, bad
+offsets).  Tolerances: tests/kda_testlib.py."""
+import numpy as np
+import pytest
+import torch
+
+import synth
+from tests.kda_testlib import compare, f64, gpu_prefill, oracle_prefill, to_device
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+
+@pytest.mark.parametrize("T", [1, 2, 15, 16, 17, 63, 64, 65, 200])
+def test_lengths_bf16_d128(kda, T):
+    inp = synth.custom(T, 3, 128, torch.bfloat16, seed=300 + T, init_std=0.01)
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, torch.bfloat16, f"out T={T}")
+    compare(fin, ref_fin, torch.bfloat16, f"state T={T}")
+
+
+@pytest.mark.parametrize("d", [16, 32, 64, 128])
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_head_sizes_and_dtypes(kda, d, dtype):
+    inp = synth.custom(150, 4, d, dtype, seed=400 + d, init_std=0.1)
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, dtype, f"out d={d}")
+    compare(fin, ref_fin, dtype, f"state d={d}")
+
+
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_packed_documents_with_empty_and_single(kda, dtype):
+    lengths = [70, 0, 1, 129, 0, 64, 3]
+    inp = synth.custom(sum(lengths), 2, 128, dtype, seed=500, lengths=lengths, init_std=0.05)
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, dtype, "out varlen")
+    compare(fin, ref_fin, dtype, "state varlen")
+    # an empty document hands its initial state straight back
+    assert torch.equal(fin[1].cpu(), inp["init_state"][1])
+
+
+def test_all_documents_empty(kda):
+    H, d = 2, 64
+    s0 = torch.randn(3, H, d, d, device="cuda")
+    e = torch.empty(0, H, d, device="cuda", dtype=torch.bfloat16)
+    ef = torch.empty(0, H, d, device="cuda")
+    out, fin = kda.kda_prefill(e, e, e, ef, torch.empty(0, H, device="cuda"), s0,
+                               torch.zeros(4, dtype=torch.int32, device="cuda"))
+    assert out.numel() == 0 and torch.equal(fin, s0)
+
+
+def test_split_run_carries_state(kda):
+    """prefill(T1) then prefill(T2) from its final state == prefill(T1+T2)."""
+    inp = to_device(synth.custom(300, 2, 128, torch.bfloat16, seed=502, init_std=0.05))
+    out, fin = gpu_prefill(kda, inp)
+    a = {k: (v[:130] if isinstance(v, torch.Tensor) and k != "init_state" else v)
+         for k, v in inp.items()}
+    a["cu_seqlens"] = np.array([0, 130])
+    b = {k: (v[130:] if isinstance(v, torch.Tensor) and k != "init_state" else v)
+         for k, v in inp.items()}
+    b["cu_seqlens"] = np.array([0, 170])
+    out_a, fin_a = gpu_prefill(kda, a)
+    b["init_state"] = fin_a
+    out_b, fin_b = gpu_prefill(kda, b)
+    compare(torch.cat([out_a, out_b]), f64(out), torch.bfloat16, "split out")
+    compare(fin_b, f64(fin), torch.bfloat16, "split state")
+
+
+def test_final_state_may_alias_init_state(kda):
+    inp = synth.custom(97, 2, 128, torch.bfloat16, seed=503, init_std=0.05)
+    d = to_device(inp)
+    ref_out, ref_fin = oracle_prefill(inp)
+    state = d["init_state"].clone()
+    out, fin = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state, None,
+                               final_state=state)
+    compare(state, ref_fin, torch.bfloat16, "aliased state")
+    compare(out, ref_out, torch.bfloat16, "aliased out")
+
+
+def test_bad_offsets_set_the_device_status(kda):
+    inp = to_device(synth.custom(40, 2, 64, torch.bfloat16, seed=504))
+    ws = torch.zeros(kda.kda_prefill_workspace_size(2, 64, torch.bfloat16, 40, 2),
+                     dtype=torch.uint8, device="cuda")
+    bad = torch.tensor([0, 30, 20], dtype=torch.int32, device="cuda")   # decreasing
+    kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, bad,
+                    workspace=ws)
+    assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_BAD_OFFSETS
+    good = torch.tensor([0, 20, 40], dtype=torch.int32, device="cuda")
+    kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, good,
+                    workspace=ws)
+    assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_OK

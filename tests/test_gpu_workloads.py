@@ -1,0 +1,74 @@
+"""The five KDA workloads at full size, in the launch configuration the
+benchmark times, against the fp64 oracle.  Where the oracle would take
+minutes (packed and long-context workloads) it runs on a few sampled heads:
+heads are independent, so a sampled head is checked element by element over
+all of its tokens.  Tolerances: tests/kda_testlib.py."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from tests.kda_testlib import compare, f64, gpu_prefill, oracle_prefill, to_device
+
+pytestmark = [pytest.mark.gpu,
+              pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
+
+
+def test_workload1_tiny_fp32(kda):
+    inp = synth.inputs(1)
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, torch.float32, "w1 out")
+    compare(fin, ref_fin, torch.float32, "w1 state")
+
+
+def test_workload2_single_sequence(kda):
+    inp = synth.inputs(2)
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, torch.bfloat16, "w2 out")
+    compare(fin, ref_fin, torch.bfloat16, "w2 state")
+
+
+def test_workload3_packed_documents(kda):
+    heads = [0, 41, 95]
+    dev = synth.inputs(3, device="cuda")
+    out, fin = gpu_prefill(kda, dev)
+    ref_out, ref_fin = oracle_prefill(synth.inputs(3, heads=heads))
+    compare(out[:, heads], ref_out, torch.bfloat16, "w3 out (sampled heads)")
+    compare(fin[:, heads], ref_fin, torch.bfloat16, "w3 state (sampled heads)")
+
+
+def test_workload4_long_context_with_prologue(kda):
+    heads = [0, 77]
+    dev = synth.inputs(4, device="cuda")
+    T = dev["q_raw"].shape[0]
+    q, k, v, g, b = kda.kda_prologue(dev["q_raw"], dev["k_raw"], dev["v_raw"], dev["conv_w"],
+                                     dev["z_g"], dev["z_beta"], None)
+    del dev
+    assert bool(((g >= -5) & (g <= 0)).all())
+    out, fin = kda.kda_prefill(q, k, v, g, b, None, None)
+    host = synth.inputs(4, heads=heads)
+    rq, rk, rv, rg, rb = oracle.prologue(f64(host["q_raw"]), f64(host["k_raw"]),
+                                         f64(host["v_raw"]), f64(host["conv_w"]),
+                                         f64(host["z_g"]), f64(host["z_beta"]), None)
+    compare(q[:, heads], rq, torch.bfloat16, "w4 prologue q")
+    compare(k[:, heads], rk, torch.bfloat16, "w4 prologue k")
+    compare(v[:, heads], rv, torch.bfloat16, "w4 prologue v")
+    compare(g[:, heads], rg, torch.float32, "w4 prologue g")
+    compare(b[:, heads], rb, torch.float32, "w4 prologue beta")
+    ref_out, ref_fin = oracle.recurrence(rq, rk, rv, rg, rb)
+    compare(out[:, heads], ref_out, torch.bfloat16, "w4 out (sampled heads)")
+    compare(fin[:, heads], ref_fin, torch.bfloat16, "w4 state (sampled heads)")
+    assert out.shape == (T, 96, 128)
+
+
+def test_workload5_decode(kda):
+    inp = synth.inputs(5)
+    dv = to_device(inp)
+    state = dv["init_state"]
+    out = kda.kda_decode_step(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], state)
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, torch.bfloat16, "w5 out")
+    compare(state, ref_fin, torch.bfloat16, "w5 state")
