@@ -185,6 +185,9 @@ def roofline(bytes_per_launch, launch_ms, peak_gbs, traffic=None):
 
 def bench_prefill(kda, synth, dist, args, peaks):
     inp = synth.inputs(2, device="cuda")
+    if args.prefill_tokens:
+        inp = {k: (v[:args.prefill_tokens].contiguous() if isinstance(v, torch.Tensor) else v)
+               for k, v in inp.items()}
     T = inp["q"].shape[0]
     out = torch.empty_like(inp["v"])
     fin = torch.empty(1, H, D, D, dtype=torch.float32, device="cuda")
@@ -229,6 +232,9 @@ def bench_prefill(kda, synth, dist, args, peaks):
 
 def bench_decode(kda, synth, dist, args, peaks):
     inp = synth.inputs(5, device="cuda")
+    if args.decode_seqs:
+        inp = {k: (v[:args.decode_seqs].contiguous() if isinstance(v, torch.Tensor) else v)
+               for k, v in inp.items()}
     N = inp["q"].shape[0]
     state = inp["init_state"]
     out = torch.empty_like(inp["v"])
@@ -335,6 +341,10 @@ def main():
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    # smaller cases for profiler captures (the printed line then describes them)
+    ap.add_argument("--only", choices=["prefill", "decode", "long"])
+    ap.add_argument("--prefill-tokens", type=int, default=0)
+    ap.add_argument("--decode-seqs", type=int, default=0)
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -348,6 +358,15 @@ def main():
     from linear_attention_03_gb300 import kda
 
     peaks = load_peaks()
+    if args.only:
+        run = {"prefill": lambda: bench_prefill(kda, synth, dist, args, peaks),
+               "decode": lambda: bench_decode(kda, synth, dist, args, peaks),
+               "long": lambda: bench_long(kda, dist, args, peaks)}[args.only]
+        res = run()
+        if dist.rank == 0:
+            print(json.dumps({"only": args.only, "result": res}), flush=True)
+        dist.close()
+        return 0
     clocks = ClockSampler(dist.local)
     clocks.start()
     pre = bench_prefill(kda, synth, dist, args, peaks)

@@ -23,7 +23,8 @@
  * Conventions shared by every entry point
  *   - All tensor arguments are DEVICE pointers owned by the caller; the
  *     library never allocates, frees or keeps them.  Tensors are dense,
- *     row-major and 16-byte aligned.
+ *     row-major and 16-byte aligned, except beta / z_beta ([T, H] fp32,
+ *     read element by element), which need only 4-byte alignment.
  *   - Layouts:  q, k, g   [T, H, d_k]      v, out  [T, H, d_v]
  *               beta      [T, H]           states  [N, H, d_k, d_v] fp32
  *               cu_seqlens [N + 1] int32: document n owns tokens

@@ -43,6 +43,14 @@ kda_status need(const void *p, const char *name) {
     return KDA_OK;
 }
 
+// beta is read element by element: its natural 4-byte alignment suffices
+kda_status need4(const void *p, const char *name) {
+    if (p == nullptr) return fail(KDA_ERR_INVALID, "%s must not be NULL", name);
+    if ((reinterpret_cast<uintptr_t>(p) & 3u) != 0)
+        return fail(KDA_ERR_INVALID, "%s must be 4-byte aligned", name);
+    return KDA_OK;
+}
+
 kda_status maybe(const void *p, const char *name) {
     if (p != nullptr && !aligned16(p))
         return fail(KDA_ERR_INVALID, "%s must be 16-byte aligned", name);
@@ -91,7 +99,7 @@ kda_status kda_prefill(const void *q, const void *k, const void *v,
         KDA_TRY(need(k, "k"));
         KDA_TRY(need(v, "v"));
         KDA_TRY(need(g, "g"));
-        KDA_TRY(need(beta, "beta"));
+        KDA_TRY(need4(beta, "beta"));
         KDA_TRY(need(out, "out"));
     }
     KDA_TRY(maybe(init_state, "init_state"));
@@ -124,7 +132,7 @@ kda_status kda_decode_step(const void *q, const void *k, const void *v,
     KDA_TRY(need(k, "k"));
     KDA_TRY(need(v, "v"));
     KDA_TRY(need(g, "g"));
-    KDA_TRY(need(beta, "beta"));
+    KDA_TRY(need4(beta, "beta"));
     KDA_TRY(need(state, "state"));
     KDA_TRY(need(out, "out"));
     cudaError_t err = kda::launch_decode(q, k, v, g, beta, state, out, N, dims.H, dims.d_k,
@@ -155,11 +163,10 @@ kda_status kda_prologue(const void *q_raw, const void *k_raw,
     KDA_TRY(need(k, "k"));
     KDA_TRY(need(v, "v"));
     KDA_TRY(maybe(z_g, "z_g"));
-    KDA_TRY(maybe(z_beta, "z_beta"));
+    if (z_beta != nullptr) KDA_TRY(need4(z_beta, "z_beta"));
     KDA_TRY(maybe(cu_seqlens, "cu_seqlens"));
     if (z_g != nullptr) KDA_TRY(need(g, "g"));
-    if (z_beta != nullptr && beta == nullptr)
-        return fail(KDA_ERR_INVALID, "beta must not be NULL when z_beta is given%s");
+    if (z_beta != nullptr) KDA_TRY(need4(beta, "beta"));
     cudaError_t err = kda::launch_prologue(q_raw, k_raw, v_raw, conv_w, z_g, z_beta,
                                            cu_seqlens, N, T, dims.H, dims.d_k,
                                            (kda_dtype)dims.qkv_dtype, q, k, v, g, beta,

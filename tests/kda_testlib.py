@@ -3,10 +3,12 @@ binding, run the fp64 oracle on the same inputs, compare.
 
 Tolerances (written here once, used by every parity test):
   * fp32 inputs: max |gpu - oracle| <= 1e-4 (absolute), outputs and states.
-  * bf16 inputs, fp32 state: max |gpu - oracle| <= 2e-2 * RMS(oracle),
-    separately for the outputs and for the final states.  The reading is
-    the stricter one of "2e-2 relative to output RMS": a max-abs error, not
-    an RMS error, is held to the bound.
+  * bf16 inputs, fp32 state: RMS(gpu - oracle) <= 2e-2 * RMS(oracle) ("2e-2
+    relative to output RMS"), and in addition max |gpu - oracle| <= 2e-2 *
+    max |oracle|, separately for the outputs and for the final states.
+    A max-abs error held to 2e-2 * RMS cannot be met by any bf16 output:
+    rounding an output to bf16 alone costs up to 2^-8 of its magnitude, and
+    the largest outputs reach ~12x the RMS (measured on the smoke inputs).
 """
 import numpy as np
 import torch
@@ -34,13 +36,20 @@ def compare(got, ref, dtype, what):
     got, ref = f64(got), f64(ref)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
-    err = float(np.max(np.abs(got - ref))) if ref.size else 0.0
+    if not ref.size:
+        return 0.0, 0.0
+    diff = np.abs(got - ref)
+    err = float(diff.max())
     if dtype == torch.float32:
         bound = TOL_F32_ABS
-    else:
-        bound = TOL_BF16_REL_RMS * rms(ref)
-    assert err <= bound, f"{what}: max|err| = {err:.3e} > {bound:.3e} (rms ref {rms(ref):.3e})"
-    return err, bound
+        assert err <= bound, f"{what}: max|err| = {err:.3e} > {bound:.3e}"
+        return err, bound
+    rel = rms(diff) / max(rms(ref), 1e-30)
+    assert rel <= TOL_BF16_REL_RMS, \
+        f"{what}: RMS(err)/RMS(ref) = {rel:.3e} > {TOL_BF16_REL_RMS:.0e}"
+    bound = TOL_BF16_REL_RMS * float(np.abs(ref).max())
+    assert err <= bound, f"{what}: max|err| = {err:.3e} > 2e-2 * max|ref| = {bound:.3e}"
+    return rel, TOL_BF16_REL_RMS
 
 
 def oracle_prefill(inp, heads=None, threads=0):
