@@ -2,6 +2,7 @@
 // path selection and kernel launches.  No allocation happens here; every
 // buffer belongs to the caller.
 #include <stdio.h>
+#include <stdlib.h>
 #include <string.h>
 
 #include <atomic>
@@ -65,6 +66,16 @@ kda_status maybe(const void *p, const char *name) {
 
 constexpr size_t kStatusBytes = 256;
 
+// KDA_PREFILL_PATH=recurrent forces the CUDA-core prefill everywhere (used to
+// cross-check the two prefill kernels on the same inputs); read once.
+bool force_recurrent() {
+    static const int v = [] {
+        const char *e = getenv("KDA_PREFILL_PATH");
+        return (e != nullptr && strcmp(e, "recurrent") == 0) ? 1 : 0;
+    }();
+    return v != 0;
+}
+
 }  // namespace
 
 void kda::count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -113,9 +124,13 @@ kda_status kda_prefill(const void *q, const void *k, const void *v,
     int32_t *status = static_cast<int32_t *>(workspace);
     cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
     if (err != cudaSuccess) return cuda_fail(err, "clearing the status word");
-    err = kda::launch_prefill_recurrent(q, k, v, g, beta, init_state, cu_seqlens, N, T,
-                                        dims.H, dims.d_k, (kda_dtype)dims.qkv_dtype, out,
-                                        final_state, status, s);
+    const kda_dtype dt = (kda_dtype)dims.qkv_dtype;
+    if (T > 0 && kda::chunk_prefill_supported(dims.d_k, dt) && !force_recurrent())
+        err = kda::launch_prefill_chunk(q, k, v, g, beta, init_state, cu_seqlens, N, T, dims.H,
+                                        out, final_state, status, s);
+    else
+        err = kda::launch_prefill_recurrent(q, k, v, g, beta, init_state, cu_seqlens, N, T,
+                                            dims.H, dims.d_k, dt, out, final_state, status, s);
     if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
     return KDA_OK;
 }

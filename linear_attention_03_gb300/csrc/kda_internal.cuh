@@ -106,4 +106,12 @@ cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      float *final_state, int32_t *status,
                                      cudaStream_t stream);
 
+// Tensor-core chunked prefill (d = 128, bf16 q/k/v).
+bool chunk_prefill_supported(int32_t D, kda_dtype dt);
+cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *init_state,
+                                 const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
+                                 void *out, float *final_state, int32_t *status,
+                                 cudaStream_t stream);
+
 }  // namespace kda
