@@ -167,6 +167,29 @@ KDA_API kda_status kda_get_device_status(const void *workspace, int32_t *status_
 KDA_API const char *kda_last_error(void);
 
 /*
+ * kda_prefill for callers that cannot allocate device memory: code embedded
+ * in an engine that owns every byte of device memory, or a serving loop that
+ * must not allocate once it has started, has no way to provide kda_prefill's
+ * workspace.  The paper has no counterpart to this entry point; it is a
+ * deployment convenience, not part of KDA.
+ * Same arguments and results as kda_prefill, minus the workspace: the
+ * library keeps a fixed 64 KiB scratch array in device memory per GPU
+ * (held until the process exits) and passes it as the workspace.  Problems
+ * whose kda_prefill_workspace_size exceeds 64 KiB return KDA_ERR_INVALID.
+ *   status_out  device int32 or NULL; receives the device status word
+ *               (KDA_DEVICE_*) of this call, in stream order.
+ * The first call on each device looks the array's address up (the device
+ * must be current) and should come before any stream capture.  Calls share
+ * the array: calls that overlap on the GPU race.  Allocates nothing: no
+ * cudaMalloc or cudaFree, no allocating library routine.
+ */
+KDA_API kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v,
+                                       const float *g, const float *beta,
+                                       const float *init_state, const int32_t *cu_seqlens,
+                                       int32_t N, int64_t T, kda_dims dims, void *out,
+                                       float *final_state, int32_t *status_out, void *stream);
+
+/*
  * Number of CUDA kernels this library has queued in this process since it
  * was loaded (all threads, all devices).  Runtime memsets/copies are not
  * counted.  Lets a caller check how many kernels a timed region launched.

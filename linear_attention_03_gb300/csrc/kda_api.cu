@@ -80,6 +80,8 @@ bool force_recurrent() {
 
 void kda::count_launches(uint64_t n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
+void kda::set_last_error(kda_status code, const char *msg) { fail(code, "%s", msg); }
+
 extern "C" {
 
 const char *kda_last_error(void) { return g_last_error; }

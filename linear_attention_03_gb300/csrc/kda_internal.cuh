@@ -81,6 +81,9 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t code) {
 // Count of kernels queued by this library (kda_kernel_launches).
 void count_launches(uint64_t n);
 
+// Record the thread's last-error text for kda_last_error().
+void set_last_error(kda_status code, const char *msg);
+
 // ------------------------------------------------------------ launchers
 // Each returns the launch error (cudaSuccess when the kernels were queued).
 
