@@ -43,8 +43,8 @@ H, D = 96, 128
 BYTES_PER_TOKEN = H * D * 2 * 3 + H * D * 4 + H * 4 + H * D * 2   # 147,840
 STATE_BYTES = H * D * D * 4                                         # 6,291,456 per document
 DECODE_BYTES_PER_SEQ = H * (2 * D * D * 4 + 3 * D * 2 + D * 4 + 4 + D * 2)  # 96 * 132,612
-# recurrent-form flops per token and head: two column reductions + the update
-FLOPS_PER_TOKEN_HEAD = 6 * D * D
+# standalone prologue: raw q,k,v + z_g + z_beta in; q,k,v + g + beta out
+PROLOGUE_BYTES_PER_TOKEN = 2 * (H * D * 2 * 3 + H * D * 4 + H * 4)           # 246,528
 
 
 def load_peaks():
@@ -174,6 +174,23 @@ def time_steps(dist, step, steps, warmup, counter=None):
     return (total, per, n1 - n0) if counter else (total, per)
 
 
+def traffic_for(kernel, units):
+    """DRAM bytes per launch from the committed ncu summary, scaled to `units`
+    (tokens or sequences) of this launch -- or None when the kernel's source
+    changed after the counters were taken."""
+    import hashlib
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        with open(path) as f:
+            entry = json.load(f)[kernel]
+        with open(os.path.join(ROOT, entry["source"]), "rb") as f:
+            if hashlib.sha256(f.read()).hexdigest() != entry["sha256"]:
+                return None
+        return int(entry["dram_bytes"] * units / entry["units"])
+    except (OSError, KeyError, ValueError):
+        return None
+
+
 def roofline(bytes_per_launch, launch_ms, peak_gbs, traffic=None):
     achieved = bytes_per_launch / (launch_ms * 1e-3) / 1e9
     return {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak_gbs, "unit": "GB/s",
@@ -202,7 +219,8 @@ def bench_prefill(kda, synth, dist, args, peaks):
                                                counter=kda.kda_kernel_launches)
     bytes_launch = BYTES_PER_TOKEN * T + STATE_BYTES
     res = {"total_ms": total_ms, "tokens": T, "launch_ms": statistics.mean(per),
-           "roofline": roofline(bytes_launch, statistics.mean(per), peaks["hbm_gbs"]),
+           "roofline": roofline(bytes_launch, statistics.mean(per), peaks["hbm_gbs"],
+                                traffic_for("chunk_kernel", T)),
            "gpu_launches": int(launches_timed)}
 
     # end to end: pinned host inputs -> device, prefill, outputs -> pinned host
@@ -249,11 +267,11 @@ def bench_decode(kda, synth, dist, args, peaks):
             "tokens_per_s": round(steps_s * N * dist.world, 1),
             "ms_per_step": round(total_ms / args.steps, 4),
             "roofline": roofline(DECODE_BYTES_PER_SEQ * N, statistics.mean(per),
-                                 peaks["hbm_gbs"])}
+                                 peaks["hbm_gbs"], traffic_for("decode_kernel", N))}
 
 
 def bench_long(kda, dist, args, peaks):
-    T = 262144
+    T = args.long_tokens
     g = torch.Generator(device="cuda").manual_seed(3)
     mk = lambda *s, dt=torch.float32: torch.randn(*s, generator=g, device="cuda",
                                                   dtype=torch.float32).to(dt)
@@ -267,19 +285,50 @@ def bench_long(kda, dist, args, peaks):
     ws = torch.empty(kda.kda_prefill_workspace_size(H, D, torch.bfloat16, T, 1),
                      dtype=torch.uint8, device="cuda")
 
-    def step():
+    def prologue():
         kda.kda_prologue(q_raw, k_raw, v_raw, conv_w, z_g, z_b, None, outs=(q, k, v, gg, bb))
+
+    def prefill():
         kda.kda_prefill(q, k, v, gg, bb, None, None, out=out, final_state=fin, workspace=ws)
 
     steps = max(1, min(args.steps, args.long_steps))
-    total_ms, per = time_steps(dist, step, steps, min(args.warmup, 3))
+    for _ in range(min(args.warmup, 3)):
+        prologue()
+        prefill()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    mk_ev = lambda: torch.cuda.Event(enable_timing=True)
+    t0, t1 = mk_ev(), mk_ev()
+    evs = [(mk_ev(), mk_ev(), mk_ev()) for _ in range(steps)]
+    t0.record()
+    for a, b, c in evs:
+        a.record()
+        prologue()
+        b.record()
+        prefill()
+        c.record()
+    t1.record()
+    torch.cuda.synchronize()
+    dist.barrier()
+    torch.cuda.synchronize()
+    total_ms = dist.max(t0.elapsed_time(t1))
+    pro = statistics.mean(a.elapsed_time(b) for a, b, _ in evs)
+    pre = statistics.mean(b.elapsed_time(c) for _, b, c in evs)
     bytes_step = BYTES_PER_TOKEN * T + STATE_BYTES + conv_w.numel() * 4
-    return {"workload": "long context: T=262144, H=96, d=128, raw bf16 q/k/v through the "
-                        "fused prologue, then prefill",
+    return {"workload": f"long context: T={T}, H=96, d=128, raw bf16 q/k/v through the "
+                        "prologue, then prefill",
             "value": round(dist.world * T * steps / (total_ms * 1e-3), 1), "unit": "tokens/s",
             "ms_per_step": round(total_ms / steps, 3), "steps": steps,
-            "roofline": roofline(bytes_step, statistics.mean(per), peaks["hbm_gbs"]),
-            "note": "bytes credited: raw q/k/v, z_g, z_beta in, out and final state written once"}
+            "roofline": roofline(bytes_step, pro + pre, peaks["hbm_gbs"]),
+            "note": "bytes credited: raw q/k/v, z_g, z_beta in, out and final state written "
+                    "once (the fused minimum); the prologue and the prefill run as two kernels",
+            "prologue": {"ms": round(pro, 3),
+                         "roofline": roofline(PROLOGUE_BYTES_PER_TOKEN * T + conv_w.numel() * 4,
+                                              pro, peaks["hbm_gbs"])},
+            "prefill": {"ms": round(pre, 3),
+                        "roofline": roofline(BYTES_PER_TOKEN * T + STATE_BYTES, pre,
+                                             peaks["hbm_gbs"], traffic_for("chunk_kernel", T))}}
 
 
 def cpu_baseline(synth, heads):
@@ -337,6 +386,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="kda", choices=["kda", "reference"])
     ap.add_argument("--long-steps", type=int, default=5)
+    ap.add_argument("--long-tokens", type=int, default=262144)
     ap.add_argument("--ref-heads", type=int, default=16)
     ap.add_argument("--no-long", action="store_true")
     ap.add_argument("--no-decode", action="store_true")

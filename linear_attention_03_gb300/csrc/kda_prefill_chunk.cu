@@ -29,17 +29,21 @@
 // Only 2 exponentials per (token, channel) are taken; the rest are products
 // with per-channel tile vectors.
 //
-// Data path (one CTA of 256 threads per (document, head), chunks in order):
+// Data path (one CTA of 512 threads per (document, head), chunks in order):
 //   TMA (128B swizzle) -> shared memory tiles of q, k, v (bf16) and g (fp32)
 //   CUDA cores: cumulative G, decay factors, bf16 operands in shared memory
 //   tcgen05.mma (bf16 x bf16 -> fp32 in TMEM) for every matrix product
 //   CUDA cores: UT solve in fp32 (16x16 diagonal blocks by forward
 //               substitution, off-diagonal blocks by block recursion)
-//   the fp32 state lives in registers (64 values per thread); its bf16 copy
-//   in shared memory is the B operand of the next chunk's W S / Q+ S.
+//   the fp32 state lives in TMEM; its bf16 copy in shared memory is the B
+//   operand of the next chunk's W S / Q+ S.
+// Decay factors are 2^x of log2-scaled G on the special-function unit; the
+// operand scalings are packed bf16x2 products (the operands are bf16 anyway).
 // All waits are bounded: a lost arrival sets KDA_DEVICE_TIMEOUT and the CTA
 // leaves after draining its own outstanding copies.
 #include <cuda.h>
+
+#include <type_traits>
 
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
@@ -51,37 +55,42 @@ using namespace tc;
 
 constexpr int kC = 64;         // tokens per chunk
 constexpr int kD = 128;        // d_k = d_v
-constexpr int kThreads = 256;  // 8 warps
+constexpr int kThreads = 512;  // 16 warps: 4 per TMEM sub-partition
+constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-// A1: [-W ; Q+] K-major, two K halves of [128 rows][128 B]; the q tile of
-//     the chunk is loaded by TMA into rows 64..127 and scaled in place.
+// A1: [-W ; Q+] K-major, two K halves of [128 rows][128 B].  The q tile of a
+//     chunk is loaded by TMA into rows 64..127 and scaled in place; rows
+//     0..63 hold K+ (MN-major, channel halves 16 KB apart) until W replaces it.
 constexpr uint32_t OFF_A1 = 0;
-// k tile (TMA, channel halves of [64 rows][128 B]) -> K+ in place (MN-major B)
-constexpr uint32_t OFF_K = 32768;
-// v tile (TMA) -- used directly as the MN-major B operand of Ut = Tb V
-constexpr uint32_t OFF_V = 49152;
-// g tile fp32 [64][128] (TMA, no swizzle) -> G in place -> Khat (MN-major A,
-// channel halves of [64 rows][128 B]) after the operand pass
+// two tile buffers that alternate roles: chunk c loads k into BUF[c & 1]
+// (turned into Khat in place, the MN-major A operand of Khat^T U) and v into
+// BUF[(c + 1) & 1] (the MN-major B operand of Ut = Tb V as loaded)
+constexpr uint32_t OFF_BUF0 = 32768;
+constexpr uint32_t OFF_BUF1 = 49152;
+// g tile fp32 [64][128] (TMA, no swizzle) -> log2e * G in place
 constexpr uint32_t OFF_G = 65536;
-// Gram region: operands of the Gram MMAs, then P / L / Tb / U
+// Gram region: cumsum scratch, the Gram operands, afterwards P / L / Tb / U
 constexpr uint32_t OFF_GR = 98304;
+constexpr uint32_t GR_CS = 0;          // fp32 [16][128] partial sums of the cumsum
 constexpr uint32_t GR_GA = 0;          // [kE; qE] K-major, 2 halves x 16384
-constexpr uint32_t GR_RT = 32768;      // R^(a), a = 0..3 (4K, 8K, 12K, 16K)
+constexpr uint32_t GR_RT = 32768;      // R rows 0..159 K-major, 2 halves x 20480
+constexpr uint32_t RT_HALF = 20480;
 constexpr uint32_t GR_P = 0;           // [0; P] K-major [128][128 B]
-constexpr uint32_t GR_L = 16384;       // L, then T, fp32 [64][64]
-constexpr uint32_t GR_TB = 32768;      // [Tb; 0] K-major [128][128 B]
-constexpr uint32_t GR_U = 49152;       // U MN-major, 2 halves of [64][128 B]
-constexpr uint32_t GR_Y = 65536;       // fp32 [16][48] scratch of the UT solve
-// bf16 state, MN-major B: two N halves of [128 rows][128 B]
+constexpr uint32_t GR_L = 16384;       // L, then T: fp32 [64][LST]
+constexpr uint32_t LST = 68;           // padded row stride (floats)
+constexpr uint32_t GR_TB = 34816;      // [Tb; 0] K-major [128][128 B]
+constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]
+constexpr uint32_t GR_Y = 67584;       // fp32 [16][48] scratch of the UT solve
+// bf16 copy of the state, MN-major B: two N halves of [128 rows][128 B]
 constexpr uint32_t OFF_S = 172032;
-// per-channel fp32 vectors of the chunk
+// per-channel vectors of the chunk
 constexpr uint32_t OFF_VEC = 204800;
-constexpr uint32_t VEC_GS = 0;                 // [4][128] e^{s_a}
-constexpr uint32_t VEC_KH = 4 * 512;           // [4][128] e^{G_63 - e_a}
-constexpr uint32_t VEC_PV = 8 * 512;           // [10][128] e^{s_a - e_b}, b <= a
-constexpr uint32_t VEC_DEC = 18 * 512;         // [128] e^{G_63}
-constexpr uint32_t OFF_BETA = OFF_VEC + 19 * 512;   // [64] fp32
+constexpr uint32_t VEC_GS = 0;          // bf16 [4][128]  e^{s_a}
+constexpr uint32_t VEC_KH = 1024;       // bf16 [4][128]  e^{G_63 - e_a}
+constexpr uint32_t VEC_PV = 2048;       // bf16 [10][128] e^{s_a - e_b}, b <= a
+constexpr uint32_t VEC_DEC = 4608;      // fp32 [128]     e^{G_63}
+constexpr uint32_t OFF_BETA = OFF_VEC + 5120;       // [64] fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;        // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 64;         // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
@@ -91,16 +100,25 @@ constexpr uint32_t BAR_Q = 0, BAR_K = 8, BAR_V = 16, BAR_G = 24, BAR_MMA = 32;
 
 // TMEM columns
 constexpr uint32_t TM_D1 = 0;     // [U ; O] accumulator
-constexpr uint32_t TM_D3 = 128;   // Khat^T U
-constexpr uint32_t TM_G = 256;    // Gram blocks (160 columns), then W (128)
+constexpr uint32_t TM_G = 128;    // Gram blocks (160 columns), then W, then Khat^T U
+constexpr uint32_t TM_D3 = 128;
+constexpr uint32_t TM_S = 288;    // fp32 state, 128 columns
 constexpr uint32_t TM_COLS = 512;
 
-__device__ __forceinline__ uint32_t gram_col(int a) { return 8u * a * (a + 1); }  // 0,16,48,96
-__device__ __forceinline__ uint32_t rt_off(int a) { return 2048u * a * (a + 1); }  // 0,4K,12K,24K
+// first row / column of row tile a inside the stacked Gram operand / result
+__device__ __forceinline__ uint32_t gram_off(int a) { return 8u * a * (a + 1); }  // 0,16,48,96
+__device__ __forceinline__ uint32_t buf_off(int i) { return (i & 1) ? OFF_BUF1 : OFF_BUF0; }
 
 struct Maps {
     CUtensorMap q, k, v, g;
 };
+
+__device__ __forceinline__ void load8f(const uint8_t *p, float (&x)[8]) {
+    const float4 a = reinterpret_cast<const float4 *>(p)[0];
+    const float4 b = reinterpret_cast<const float4 *>(p)[1];
+    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+}
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
@@ -113,13 +131,13 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sp = warp & 3;          // TMEM sub-partition (lanes 32*sp .. 32*sp+31)
-    const int hh = warp >> 2;         // which 64-column half this warp handles
+    const int qq = warp >> 2;         // which 32-column quarter this warp handles
     const int h = blockIdx.x, n = blockIdx.y;
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC);
-    // plain shared-memory accesses (the compiler may schedule them) by address
-#define SM_F(a) (*reinterpret_cast<float *>(smem + ((a) - sb)))
-#define SM_F4(a) (*reinterpret_cast<float4 *>(smem + ((a) - sb)))
-#define SM_U4(a) (*reinterpret_cast<uint4 *>(smem + ((a) - sb)))
+#define SM_F(o) (*reinterpret_cast<float *>(smem + (o)))
+#define SM_F4(o) (*reinterpret_cast<float4 *>(smem + (o)))
+#define SM_U4(o) (*reinterpret_cast<uint4 *>(smem + (o)))
+#define SM_H(o) (*reinterpret_cast<__nv_bfloat16 *>(smem + (o)))
 
     int64_t bos, eos;
     if (!doc_bounds(cu, n, N, T, bos, eos)) {
@@ -136,32 +154,38 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sb + OFF_MISC, TM_COLS);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = misc[0];
+    const uint32_t tlane = tmem + ((uint32_t)(32 * sp) << 16);   // this warp's lanes
 
-    // state rows r = 32*sp + lane, columns 64*hh .. 64*hh+63, fp32 registers
+    // the state: row r = 32*sp + lane, columns 32*qq .. 32*qq+31, fp32 in TMEM
+    // and bf16 in shared memory (N half qq >> 1, 16-byte chunks 4*(qq & 1) + i)
     const int srow = 32 * sp + lane;
-    float S[64];
+    const uint32_t s_smem = OFF_S + (qq >> 1) * 16384;
     {
-        const float *src = init_state ? init_state + unit * kD * kD + (size_t)srow * kD + 64 * hh
+        float S[32];
+        const float *src = init_state ? init_state + unit * kD * kD + (size_t)srow * kD + 32 * qq
                                       : nullptr;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4) {
+        for (int j = 0; j < 32; j += 4) {
             float4 x = src ? *reinterpret_cast<const float4 *>(src + j)
                            : make_float4(0.f, 0.f, 0.f, 0.f);
             S[j] = x.x; S[j + 1] = x.y; S[j + 2] = x.z; S[j + 3] = x.w;
         }
+        tmem_st32(tlane + TM_S + 32 * qq, S);
 #pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
+        for (int i = 0; i < 4; ++i) {
             float x[8];
 #pragma unroll
-            for (int e = 0; e < 8; ++e) x[e] = S[8 * c8 + e];
-            (SM_U4(sb + OFF_S + hh * 16384 + sw128_off(srow, c8)) = pack_bf16x8(x));
+            for (int e = 0; e < 8; ++e) x[e] = S[8 * i + e];
+            SM_U4(s_smem + sw128_off(srow, 4 * (qq & 1) + i)) = pack_bf16x8(x);
         }
     }
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = misc[0];
 
     auto issue_q = [&](int64_t t0) {
         mbar_expect_tx(sb + OFF_BAR + BAR_Q, 16384);
@@ -169,15 +193,15 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         tma_load_2d(sb + OFF_A1 + 16384 + 8192, &maps.q, h * kD + 64, (int32_t)t0,
                     sb + OFF_BAR + BAR_Q);
     };
-    auto issue_k = [&](int64_t t0) {
+    auto issue_k = [&](int64_t t0, uint32_t buf) {
         mbar_expect_tx(sb + OFF_BAR + BAR_K, 16384);
-        tma_load_2d(sb + OFF_K, &maps.k, h * kD, (int32_t)t0, sb + OFF_BAR + BAR_K);
-        tma_load_2d(sb + OFF_K + 8192, &maps.k, h * kD + 64, (int32_t)t0, sb + OFF_BAR + BAR_K);
+        tma_load_2d(sb + buf, &maps.k, h * kD, (int32_t)t0, sb + OFF_BAR + BAR_K);
+        tma_load_2d(sb + buf + 8192, &maps.k, h * kD + 64, (int32_t)t0, sb + OFF_BAR + BAR_K);
     };
-    auto issue_v = [&](int64_t t0) {
+    auto issue_v = [&](int64_t t0, uint32_t buf) {
         mbar_expect_tx(sb + OFF_BAR + BAR_V, 16384);
-        tma_load_2d(sb + OFF_V, &maps.v, h * kD, (int32_t)t0, sb + OFF_BAR + BAR_V);
-        tma_load_2d(sb + OFF_V + 8192, &maps.v, h * kD + 64, (int32_t)t0, sb + OFF_BAR + BAR_V);
+        tma_load_2d(sb + buf, &maps.v, h * kD, (int32_t)t0, sb + OFF_BAR + BAR_V);
+        tma_load_2d(sb + buf + 8192, &maps.v, h * kD + 64, (int32_t)t0, sb + OFF_BAR + BAR_V);
     };
     auto issue_g = [&](int64_t t0) {
         mbar_expect_tx(sb + OFF_BAR + BAR_G, 32768);
@@ -189,11 +213,14 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
     int issued[4] = {-1, -1, -1, -1};
     if (tid == 0 && nchunks > 0) {
         issue_q(bos);
-        issue_k(bos);
-        issue_v(bos);
+        issue_k(bos, buf_off(0));
+        issue_v(bos, buf_off(1));
         issue_g(bos);
         issued[0] = issued[1] = issued[2] = issued[3] = 0;
     }
+    // beta of the next chunk, held in a register by threads 0..63
+    float beta_next = 0.f;
+    if (tid < kC && nchunks > 0 && tid < len) beta_next = beta[(size_t)(bos + tid) * H + h];
 
     uint32_t mma_phase = 0;
     // all threads wait on the MMA barrier; a timeout raises the abort flag
@@ -206,39 +233,46 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         if (!mbar_wait(sb + OFF_BAR + bar, c & 1)) misc[1] = 1;
     };
 
-    const uint32_t gr = sb + OFF_GR;
+    const uint32_t gr = sb + OFF_GR;    // shared address of the Gram region (descriptors)
     int c = 0;
     for (; c < nchunks; ++c) {
         const int64_t t0 = bos + (int64_t)c * kC;
         const int lenc = (eos - t0) < kC ? static_cast<int>(eos - t0) : kC;
+        const uint32_t kbuf = buf_off(c), vbuf = buf_off(c + 1);
 
-        // ---------------- step 1: inputs, beta, cumulative log-decay
+        // ---------------- step 1: inputs, beta, cumulative log-decay (log2 units)
+        if (tid < kC) SM_F(OFF_BETA + 4 * tid) = beta_next;
         wait_tma(BAR_Q, c);
         wait_tma(BAR_K, c);
         wait_tma(BAR_G, c);
-        if (tid < kC)
-            (SM_F(sb + OFF_BETA + 4 * tid) = tid < lenc ? beta[(size_t)(t0 + tid) * H + h] : 0.f);
         {
-            // G in place: thread = (channel, half of the tokens); 32 loads in flight
-            const int ch = tid & 127, half = tid >> 7;
-            float gv[32];
+            // thread = (4 channels, 4 tokens); two-level scan over the 16 token groups
+            const int c4 = tid & 31, tg = tid >> 5;
+            float4 x[4];
 #pragma unroll
-            for (int i = 0; i < 32; ++i) {
-                const int t = 32 * half + i;
-                gv[i] = (t < lenc) ? SM_F(sb + OFF_G + (uint32_t)(t * kD + ch) * 4) : 0.f;
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * tg + i;
+                x[i] = (t < lenc) ? SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4)
+                                  : make_float4(0.f, 0.f, 0.f, 0.f);
             }
 #pragma unroll
-            for (int i = 1; i < 32; ++i) gv[i] += gv[i - 1];
-            if (half == 0) {
-#pragma unroll
-                for (int i = 0; i < 32; ++i) SM_F(sb + OFF_G + (uint32_t)(i * kD + ch) * 4) = gv[i];
+            for (int i = 1; i < 4; ++i) {
+                x[i].x += x[i - 1].x; x[i].y += x[i - 1].y;
+                x[i].z += x[i - 1].z; x[i].w += x[i - 1].w;
             }
+            SM_F4(OFF_GR + GR_CS + (uint32_t)(tg * kD + 4 * c4) * 4) = x[3];
             __syncthreads();
-            if (half == 1) {
-                const float base = SM_F(sb + OFF_G + (uint32_t)(31 * kD + ch) * 4);
+            float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int g2 = 0; g2 < tg; ++g2) {
+                const float4 p = SM_F4(OFF_GR + GR_CS + (uint32_t)(g2 * kD + 4 * c4) * 4);
+                off.x += p.x; off.y += p.y; off.z += p.z; off.w += p.w;
+            }
 #pragma unroll
-                for (int i = 0; i < 32; ++i)
-                    SM_F(sb + OFF_G + (uint32_t)((32 + i) * kD + ch) * 4) = gv[i] + base;
+            for (int i = 0; i < 4; ++i) {
+                const int t = 4 * tg + i;
+                SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4) =
+                    make_float4((x[i].x + off.x) * kLog2e, (x[i].y + off.y) * kLog2e,
+                                (x[i].z + off.z) * kLog2e, (x[i].w + off.w) * kLog2e);
             }
         }
         __syncthreads();
@@ -246,264 +280,261 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 
         // ---------------- per-channel tile vectors
         {
-            const int ch = tid & 127;
-            auto G = [&](int t) {
-                return t < 0 ? 0.f : SM_F(sb + OFF_G + (uint32_t)(t * kD + ch) * 4);
-            };
+            const int ch = tid & 127, part = tid >> 7;
+            auto G = [&](int t) { return t < 0 ? 0.f : SM_F(OFF_G + (uint32_t)(t * kD + ch) * 4); };
             const float g63 = G(63);
-            if (tid < 128) {
+            if (part == 0) {
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    (SM_F(sb + OFF_VEC + VEC_GS + a * 512 + ch * 4) = __expf(G(16 * a - 1)));
-                    (SM_F(sb + OFF_VEC + VEC_KH + a * 512 + ch * 4) = __expf(g63 - G(16 * a + 15)));
-                }
-                (SM_F(sb + OFF_VEC + VEC_DEC + ch * 4) = __expf(g63));
+                for (int a = 0; a < 4; ++a)
+                    SM_H(OFF_VEC + VEC_GS + a * 256 + ch * 2) = __float2bfloat16_rn(ex2(G(16 * a - 1)));
+                SM_F(OFF_VEC + VEC_DEC + ch * 4) = ex2(g63);
+            } else if (part == 1) {
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+                    SM_H(OFF_VEC + VEC_KH + a * 256 + ch * 2) =
+                        __float2bfloat16_rn(ex2(g63 - G(16 * a + 15)));
             } else {
+                // pairs (a, b <= a) in order; part 2 takes 0..4, part 3 takes 5..9
 #pragma unroll
                 for (int a = 0; a < 4; ++a)
 #pragma unroll
-                    for (int b = 0; b <= a; ++b)
-                        (SM_F(sb + OFF_VEC + VEC_PV + (a * (a + 1) / 2 + b) * 512 + ch * 4) = __expf(G(16 * a - 1) - G(16 * b + 15)));
+                    for (int b = 0; b <= a; ++b) {
+                        const int idx = a * (a + 1) / 2 + b;
+                        if ((idx < 5) == (part == 2))
+                            SM_H(OFF_VEC + VEC_PV + idx * 256 + ch * 2) =
+                                __float2bfloat16_rn(ex2(G(16 * a - 1) - G(16 * b + 15)));
+                    }
             }
         }
         __syncthreads();
 
-        // ---------------- step 2: operands (thread: channel chunk cc, one row per tile)
-        uint4 khat[4];
+        // ---------------- step 2: operands.  thread = (row tile a, 2 rows, 8 channels)
         {
-            const int cc = tid & 15;                 // 8-channel chunk
-            const int half = cc >> 3, c8 = cc & 7;   // channel half, chunk in the half
-            const int c0 = 8 * cc;
+            const int a = tid >> 7, r2 = (tid >> 4) & 7, cc = tid & 15;
+            const int half = cc >> 3, c8 = cc & 7, c0 = 8 * cc;
+            float Gs[8], Ge[8];
+            if (a == 0) {
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const int t = (tid >> 4) + 16 * a;
-                const bool live = t < lenc;
-                float Gt[8], Gs[8], Ge[8];
-                {
-                    const uint32_t rt = sb + OFF_G + (uint32_t)(t * kD + c0) * 4;
-                    float4 x0 = SM_F4(rt), x1 = SM_F4(rt + 16);
-                    Gt[0] = x0.x; Gt[1] = x0.y; Gt[2] = x0.z; Gt[3] = x0.w;
-                    Gt[4] = x1.x; Gt[5] = x1.y; Gt[6] = x1.z; Gt[7] = x1.w;
-                    const uint32_t re = sb + OFF_G + (uint32_t)((16 * a + 15) * kD + c0) * 4;
-                    x0 = SM_F4(re); x1 = SM_F4(re + 16);
-                    Ge[0] = x0.x; Ge[1] = x0.y; Ge[2] = x0.z; Ge[3] = x0.w;
-                    Ge[4] = x1.x; Ge[5] = x1.y; Ge[6] = x1.z; Ge[7] = x1.w;
-                    if (a == 0) {
+                for (int e = 0; e < 8; ++e) Gs[e] = 0.f;
+            } else {
+                load8f(smem + OFF_G + (uint32_t)((16 * a - 1) * kD + c0) * 4, Gs);
+            }
+            load8f(smem + OFF_G + (uint32_t)((16 * a + 15) * kD + c0) * 4, Ge);
+            uint4 kE[2], qE[2], kB[2];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) Gs[e] = 0.f;
-                    } else {
-                        const uint32_t rs = sb + OFF_G + (uint32_t)((16 * a - 1) * kD + c0) * 4;
-                        x0 = SM_F4(rs); x1 = SM_F4(rs + 16);
-                        Gs[0] = x0.x; Gs[1] = x0.y; Gs[2] = x0.z; Gs[3] = x0.w;
-                        Gs[4] = x1.x; Gs[5] = x1.y; Gs[6] = x1.z; Gs[7] = x1.w;
-                    }
-                }
-                const uint32_t kaddr = sb + OFF_K + half * 8192 + sw128_off(t, c8);
-                const uint32_t qaddr = sb + OFF_A1 + half * 16384 + sw128_off(64 + t, c8);
-                float kv[8], qv[8];
-                unpack_bf16x8(SM_U4(kaddr), kv);
-                unpack_bf16x8(SM_U4(qaddr), qv);
-                if (!live) {
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) kv[e] = qv[e] = 0.f;
-                }
+            for (int i = 0; i < 2; ++i) {
+                const int t = 16 * a + 2 * r2 + i;
+                float Gt[8];
+                load8f(smem + OFF_G + (uint32_t)(t * kD + c0) * 4, Gt);
+                uint4 kv = SM_U4(kbuf + half * 8192 + sw128_off(t, c8));
+                uint4 qv = SM_U4(OFF_A1 + half * 16384 + sw128_off(64 + t, c8));
+                if (t >= lenc) kv = qv = make_uint4(0, 0, 0, 0);
                 float E[8], Eb[8];
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
-                    E[e] = __expf(Gt[e] - Gs[e]);
-                    Eb[e] = __expf(Ge[e] - Gt[e]);
+                    E[e] = ex2(Gt[e] - Gs[e]);
+                    Eb[e] = ex2(Ge[e] - Gt[e]);
                 }
+                const uint4 Ep = pack_bf16x8(E), Ebp = pack_bf16x8(Eb);
+                kE[i] = mul_bf16x8(kv, Ep);
+                qE[i] = mul_bf16x8(qv, Ep);
+                kB[i] = mul_bf16x8(kv, Ebp);
                 // Gram left operand rows t (k) and 64 + t (q)
-                float x[8];
+                SM_U4(OFF_GR + GR_GA + half * 16384 + sw128_off(t, c8)) = kE[i];
+                SM_U4(OFF_GR + GR_GA + half * 16384 + sw128_off(64 + t, c8)) = qE[i];
+                // Gram right operand: row gram_off(ap) + t for every row tile ap >= a
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = kv[e] * E[e];
-                (SM_U4(gr + GR_GA + half * 16384 + sw128_off(t, c8)) = pack_bf16x8(x));
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = qv[e] * E[e];
-                (SM_U4(gr + GR_GA + half * 16384 + sw128_off(64 + t, c8)) = pack_bf16x8(x));
-                // Gram right operands R^(a') for every row tile a' >= a
-                float kb[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) kb[e] = kv[e] * Eb[e];
-#pragma unroll
-                for (int ap = a; ap < 4; ++ap) {
-                    const uint32_t pv = sb + OFF_VEC + VEC_PV + (ap * (ap + 1) / 2 + a) * 512 + c0 * 4;
-                    const float4 p0 = SM_F4(pv), p1 = SM_F4(pv + 16);
-                    const float pvv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = kb[e] * pvv[e];
-                    const uint32_t nrows = 16u * (ap + 1);
-                    (SM_U4(gr + GR_RT + rt_off(ap) + half * nrows * 128 + sw128_off(t, c8)) = pack_bf16x8(x));
-                }
-                // Q+ and K+ in place: scale by e^{G_t} = E_t e^{s_a}
-                {
-                    const uint32_t gs = sb + OFF_VEC + VEC_GS + a * 512 + c0 * 4;
-                    const float4 p0 = SM_F4(gs), p1 = SM_F4(gs + 16);
-                    const float gsv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-                    float y[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const float at = E[e] * gsv[e];
-                        x[e] = qv[e] * at;
-                        y[e] = kv[e] * at;
-                    }
-                    (SM_U4(qaddr) = pack_bf16x8(x));
-                    (SM_U4(kaddr) = pack_bf16x8(y));
-                }
-                // Khat = k e^{G_63 - G_t} = (k Eb) e^{G_63 - e_a}; stored after the barrier
-                {
-                    const uint32_t kh = sb + OFF_VEC + VEC_KH + a * 512 + c0 * 4;
-                    const float4 p0 = SM_F4(kh), p1 = SM_F4(kh + 16);
-                    const float khv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) x[e] = kb[e] * khv[e];
-                    khat[a] = pack_bf16x8(x);
+                for (int ap = 0; ap < 4; ++ap) {
+                    if (ap < a) continue;
+                    const uint4 pv = SM_U4(OFF_VEC + VEC_PV + (ap * (ap + 1) / 2 + a) * 256 + c0 * 2);
+                    SM_U4(OFF_GR + GR_RT + half * RT_HALF + sw128_off(gram_off(ap) + t, c8)) =
+                        mul_bf16x8(kB[i], pv);
                 }
             }
-            __syncthreads();   // every read of G is done: the g buffer now takes Khat
+            fence_proxy_async();
+            __syncthreads();
+            // ---------------- step 3: Gram MMAs (8 instructions, N = 160), issued
+            // while the remaining operands are written; the g buffer is free
+            if (tid == 0) {
+                tc_fence_after();
+                if (c + 1 < nchunks) {
+                    issue_g(t0 + kC);
+                    issued[3] = c + 1;
+                }
+                const uint32_t id = idesc_bf16(128, 160, 0, 0);
 #pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const int t = (tid >> 4) + 16 * a;
-                (SM_U4(sb + OFF_G + half * 8192 + sw128_off(t, c8)) = khat[a]);
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = sw128_desc(gr + GR_GA + (kk >> 2) * 16384 + (kk & 3) * 32, 0, 1024);
+                    const uint64_t bd = sw128_desc(gr + GR_RT + (kk >> 2) * RT_HALF + (kk & 3) * 32, 0, 1024);
+                    mma_bf16(tmem + TM_G, ad, bd, id, kk > 0);
+                }
+                mma_commit(sb + OFF_BAR + BAR_MMA);
+            }
+            // Q+ in place, K+ into rows 0..63 of A1, Khat in place of k
+            const uint4 gs = SM_U4(OFF_VEC + VEC_GS + a * 256 + c0 * 2);
+            const uint4 kh = SM_U4(OFF_VEC + VEC_KH + a * 256 + c0 * 2);
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                const int t = 16 * a + 2 * r2 + i;
+                SM_U4(OFF_A1 + half * 16384 + sw128_off(64 + t, c8)) = mul_bf16x8(qE[i], gs);
+                SM_U4(OFF_A1 + half * 16384 + sw128_off(t, c8)) = mul_bf16x8(kE[i], gs);
+                SM_U4(kbuf + half * 8192 + sw128_off(t, c8)) = mul_bf16x8(kB[i], kh);
             }
         }
         fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---------------- step 3: Gram MMAs
-        if (tid == 0) {
-            tc_fence_after();
-#pragma unroll
-            for (int a = 0; a < 4; ++a) {
-                const uint32_t nrows = 16u * (a + 1);
-                const uint32_t id = idesc_bf16(128, nrows, 0, 0);
-#pragma unroll
-                for (int kk = 0; kk < 8; ++kk) {
-                    const uint64_t ad =
-                        sw128_desc(gr + GR_GA + (kk >> 2) * 16384 + (kk & 3) * 32, 0, 1024);
-                    const uint64_t bd = sw128_desc(
-                        gr + GR_RT + rt_off(a) + (kk >> 2) * nrows * 128 + (kk & 3) * 32, 0, 1024);
-                    mma_bf16(tmem + TM_G + gram_col(a), ad, bd, id, kk > 0);
-                }
-            }
-            mma_commit(sb + OFF_BAR + BAR_MMA);
-        }
         wait_mma();
 
         // ---------------- step 4: L (k rows) and P (q rows) out of TMEM
         {
-            // warp -> row tile a: sub-partition sp covers tokens 32*(sp&1)..+31
-            const int a = 2 * (sp & 1) + hh;
-            const bool mine = (lane >> 4) == hh;     // lanes of tile a
-            const int t = 32 * (sp & 1) + lane;      // token of this lane
-            float G[64];
-            tmem_ld64(tmem + ((uint32_t)(32 * sp) << 16) + TM_G + gram_col(a), G);
+            const int a = 2 * (sp & 1) + (qq >> 1);   // row tile this warp reads
+            const int ch2 = qq & 1;                   // 32-column half of the tile's columns
+            const bool mine = (lane >> 4) == (qq >> 1);
+            const int t = 32 * (sp & 1) + lane;       // token of this lane
+            float G[32];
+            tmem_ld32(tlane + TM_G + gram_off(a) + 32 * ch2, G);
             if (mine) {
                 if (sp < 2) {
-                    const float bt = SM_F(sb + OFF_BETA + 4 * t);
+                    const float bt = SM_F(OFF_BETA + 4 * t);
 #pragma unroll
-                    for (int j = 0; j < 64; j += 4) {
+                    for (int j = 0; j < 32; j += 4) {
+                        const int jj = 32 * ch2 + j;
                         float4 v;
-                        v.x = (j + 0 < t) ? bt * G[j + 0] : 0.f;
-                        v.y = (j + 1 < t) ? bt * G[j + 1] : 0.f;
-                        v.z = (j + 2 < t) ? bt * G[j + 2] : 0.f;
-                        v.w = (j + 3 < t) ? bt * G[j + 3] : 0.f;
-                        (SM_F4(gr + GR_L + (uint32_t)(t * 64 + j) * 4) = v);
+                        v.x = (jj + 0 < t) ? bt * G[j + 0] : 0.f;
+                        v.y = (jj + 1 < t) ? bt * G[j + 1] : 0.f;
+                        v.z = (jj + 2 < t) ? bt * G[j + 2] : 0.f;
+                        v.w = (jj + 3 < t) ? bt * G[j + 3] : 0.f;
+                        SM_F4(OFF_GR + GR_L + (uint32_t)(t * LST + jj) * 4) = v;
                     }
                 } else {
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
+                    for (int i = 0; i < 4; ++i) {
                         float x[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = (8 * c8 + e <= t) ? G[8 * c8 + e] : 0.f;
-                        (SM_U4(gr + GR_P + sw128_off(64 + t, c8)) = pack_bf16x8(x));
+                        for (int e = 0; e < 8; ++e) {
+                            const int jj = 32 * ch2 + 8 * i + e;
+                            x[e] = (jj <= t) ? G[8 * i + e] : 0.f;
+                        }
+                        SM_U4(OFF_GR + GR_P + sw128_off(64 + t, 4 * ch2 + i)) = pack_bf16x8(x);
                     }
                 }
             }
-            // rows 0..63 of [0; P] are zero
+            // rows 0..63 of [0; P] and rows 64..127 of [Tb; 0] are zero
             const uint4 z = make_uint4(0, 0, 0, 0);
-            for (int i = tid; i < 512; i += kThreads)
-                (SM_U4(gr + GR_P + sw128_off(i >> 3, i & 7)) = z);
+            SM_U4(OFF_GR + GR_P + sw128_off(tid >> 3, tid & 7)) = z;
+            SM_U4(OFF_GR + GR_TB + sw128_off(64 + (tid >> 3), tid & 7)) = z;
         }
         tc_fence_before();
         __syncthreads();
 
         // ---------------- step 5: T = (I + L)^-1 in fp32, then Tb = T diag(beta)
         {
-            const uint32_t Lb = gr + GR_L;
-            // 5a: diagonal 16x16 blocks, thread = (block a, column col)
-            float xcol[16];
-            const int a5 = tid >> 4, col = tid & 15;
+            const uint32_t Lo = OFF_GR + GR_L;
+            // 5a: diagonal 16x16 blocks by forward substitution, column-oriented:
+            // once x_i is known every later partial sum takes one FMA, so the
+            // dependency chain is one FMA per row.  thread = (block a, column col)
             if (tid < 64) {
-                float acc[16];
+                const int a5 = tid >> 4, col = tid & 15;
+                const uint32_t blk = Lo + (uint32_t)(16 * a5 * LST + 16 * a5) * 4;
+                float x[16], acc[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = 0.f;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    xcol[i] = (i == col ? 1.f : 0.f) - acc[i];
+                    x[i] = ((i == col) ? 1.f : 0.f) - acc[i];
 #pragma unroll
                     for (int k = i + 1; k < 16; ++k)
-                        acc[k] += SM_F(Lb + (uint32_t)((16 * a5 + k) * 64 + 16 * a5 + i) * 4) *
-                                  xcol[i];
+                        acc[k] += SM_F(blk + (uint32_t)(k * LST + i) * 4) * x[i];
                 }
+                __syncwarp();
+                // every thread of this warp has read its block: write T_aa in place
+#pragma unroll
+                for (int i = 0; i < 16; ++i) SM_F(blk + (uint32_t)(i * LST + col) * 4) = x[i];
             }
             __syncthreads();
-            if (tid < 64) {
+            // 5b: block rows a = 1..3.  Y_b = sum_{m=b}^{a-1} L_am T_mb, then
+            // T_ab = -T_aa Y_b.  Group g (64 threads) owns block column b = g;
+            // thread = (row r, 4-column quad q); loop bounds are compile-time.
+            const int grp = tid >> 6, r = (tid & 63) >> 2, q4 = tid & 3;
+            const uint32_t Yo = OFF_GR + GR_Y;
+            auto y_stage = [&](auto A_, auto B_) {
+                constexpr int A = decltype(A_)::value, B = decltype(B_)::value;
+                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
 #pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    (SM_F(Lb + (uint32_t)((16 * a5 + i) * 64 + 16 * a5 + col) * 4) = xcol[i]);
-            }
-            __syncthreads();
-            // 5b: block rows a = 1..3: T_ab = -T_aa sum_{m=b}^{a-1} L_am T_mb
-            const int i5 = tid >> 4, jj = tid & 15;
-            const uint32_t Yb = gr + GR_Y;
+                for (int m = B; m < A; ++m)
 #pragma unroll
-            for (int a = 1; a < 4; ++a) {
-                for (int b = 0; b < a; ++b) {
-                    float y = 0.f;
-                    for (int m = b; m < a; ++m)
+                    for (int l4 = 0; l4 < 4; ++l4) {
+                        const float4 lv = SM_F4(Lo + (uint32_t)((16 * A + r) * LST + 16 * m + 4 * l4) * 4);
+                        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
 #pragma unroll
-                        for (int l = 0; l < 16; ++l)
-                            y += SM_F(Lb + (uint32_t)((16 * a + i5) * 64 + 16 * m + l) * 4) *
-                                 SM_F(Lb + (uint32_t)((16 * m + l) * 64 + 16 * b + jj) * 4);
-                    (SM_F(Yb + (uint32_t)(i5 * 48 + 16 * b + jj) * 4) = y);
-                }
-                __syncthreads();
-                for (int b = 0; b < a; ++b) {
-                    float y = 0.f;
-#pragma unroll
-                    for (int l = 0; l < 16; ++l)
-                        y += SM_F(Lb + (uint32_t)((16 * a + i5) * 64 + 16 * a + l) * 4) *
-                             SM_F(Yb + (uint32_t)(l * 48 + 16 * b + jj) * 4);
-                    (SM_F(Lb + (uint32_t)((16 * a + i5) * 64 + 16 * b + jj) * 4) = -y);
-                }
-                __syncthreads();
-            }
-            // 5c: [Tb; 0], thread = (row t, 16-column quarter)
-            {
-                const int t = tid >> 2, qc = tid & 3;
-#pragma unroll
-                for (int hc = 0; hc < 2; ++hc) {
-                    const int c8 = 2 * qc + hc;
-                    float x[8];
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int j = 8 * c8 + e;
-                        x[e] = (j <= t) ? SM_F(Lb + (uint32_t)(t * 64 + j) * 4) *
-                                              SM_F(sb + OFF_BETA + 4 * j)
-                                        : 0.f;
+                        for (int e = 0; e < 4; ++e) {
+                            const float4 tv = SM_F4(Lo + (uint32_t)((16 * m + 4 * l4 + e) * LST + 16 * B + 4 * q4) * 4);
+                            float4 &y = (e & 1) ? y1 : y0;
+                            y.x += la[e] * tv.x; y.y += la[e] * tv.y;
+                            y.z += la[e] * tv.z; y.w += la[e] * tv.w;
+                        }
                     }
-                    (SM_U4(gr + GR_TB + sw128_off(t, c8)) = pack_bf16x8(x));
-                    (SM_U4(gr + GR_TB + sw128_off(64 + t, c8)) = make_uint4(0, 0, 0, 0));
+                SM_F4(Yo + (uint32_t)(r * 48 + 16 * B + 4 * q4) * 4) =
+                    make_float4(y0.x + y1.x, y0.y + y1.y, y0.z + y1.z, y0.w + y1.w);
+            };
+            auto t_stage = [&](auto A_, auto B_) {
+                constexpr int A = decltype(A_)::value, B = decltype(B_)::value;
+                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
+#pragma unroll
+                for (int l4 = 0; l4 < 4; ++l4) {
+                    const float4 tv = SM_F4(Lo + (uint32_t)((16 * A + r) * LST + 16 * A + 4 * l4) * 4);
+                    const float ta[4] = {tv.x, tv.y, tv.z, tv.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float4 yv = SM_F4(Yo + (uint32_t)((4 * l4 + e) * 48 + 16 * B + 4 * q4) * 4);
+                        float4 &y = (e & 1) ? y1 : y0;
+                        y.x += ta[e] * yv.x; y.y += ta[e] * yv.y;
+                        y.z += ta[e] * yv.z; y.w += ta[e] * yv.w;
+                    }
                 }
+                SM_F4(Lo + (uint32_t)((16 * A + r) * LST + 16 * B + 4 * q4) * 4) =
+                    make_float4(-(y0.x + y1.x), -(y0.y + y1.y), -(y0.z + y1.z), -(y0.w + y1.w));
+            };
+            using I0 = std::integral_constant<int, 0>;
+            using I1 = std::integral_constant<int, 1>;
+            using I2 = std::integral_constant<int, 2>;
+            using I3 = std::integral_constant<int, 3>;
+            // block row 1
+            if (grp == 0) y_stage(I1{}, I0{});
+            __syncthreads();
+            if (grp == 0) t_stage(I1{}, I0{});
+            __syncthreads();
+            // block row 2
+            if (grp == 0) y_stage(I2{}, I0{});
+            else if (grp == 1) y_stage(I2{}, I1{});
+            __syncthreads();
+            if (grp == 0) t_stage(I2{}, I0{});
+            else if (grp == 1) t_stage(I2{}, I1{});
+            __syncthreads();
+            // block row 3
+            if (grp == 0) y_stage(I3{}, I0{});
+            else if (grp == 1) y_stage(I3{}, I1{});
+            else if (grp == 2) y_stage(I3{}, I2{});
+            __syncthreads();
+            if (grp == 0) t_stage(I3{}, I0{});
+            else if (grp == 1) t_stage(I3{}, I1{});
+            else if (grp == 2) t_stage(I3{}, I2{});
+            __syncthreads();
+            // 5c: [Tb; 0] rows 0..63, thread = (row t, 8-column chunk)
+            {
+                const int t = tid >> 3, cb = tid & 7;
+                float x[8], tr[8], bb[8];
+                load8f(smem + Lo + (uint32_t)(t * LST + 8 * cb) * 4, tr);
+                load8f(smem + OFF_BETA + 32 * cb, bb);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) x[e] = (8 * cb + e <= t) ? tr[e] * bb[e] : 0.f;
+                SM_U4(OFF_GR + GR_TB + sw128_off(t, cb)) = pack_bf16x8(x);
             }
         }
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- step 6: W = Tb K+ and Ut = Tb V (Ut lands in D1 rows 0..63)
+        // ---------------- step 6: W = Tb K+ (TMEM cols 128..255), Ut = Tb V (D1 rows 0..63)
         if (tid == 0) {
             tc_fence_after();
             wait_tma(BAR_V, c);
@@ -511,27 +542,28 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t ad = sw128_desc(gr + GR_TB + kk * 32, 0, 1024);
-                mma_bf16(tmem + TM_G, ad, sw128_desc(sb + OFF_K + kk * 2048, 8192, 1024), id, kk > 0);
-            }
-#pragma unroll
-            for (int kk = 0; kk < 4; ++kk) {
-                const uint64_t ad = sw128_desc(gr + GR_TB + kk * 32, 0, 1024);
-                mma_bf16(tmem + TM_D1, ad, sw128_desc(sb + OFF_V + kk * 2048, 8192, 1024), id, kk > 0);
+                mma_bf16(tmem + TM_G, ad, sw128_desc(sb + OFF_A1 + kk * 2048, 16384, 1024), id, kk > 0);
+                mma_bf16(tmem + TM_D1, ad, sw128_desc(sb + vbuf + kk * 2048, 8192, 1024), id, kk > 0);
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
         wait_mma();
+        // v is consumed: the next chunk's k goes into its buffer
+        if (tid == 0 && c + 1 < nchunks) {
+            issue_k(t0 + kC, vbuf);
+            issued[1] = c + 1;
+        }
         // -W -> rows 0..63 of A1 (warps of sub-partitions 0 and 1)
         if (sp < 2) {
             const int t = 32 * sp + lane;
-            float v64[64];
-            tmem_ld64(tmem + ((uint32_t)(32 * sp) << 16) + TM_G + 64 * hh, v64);
+            float v32[32];
+            tmem_ld32(tlane + TM_G + 32 * qq, v32);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int i = 0; i < 4; ++i) {
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = -v64[8 * c8 + e];
-                (SM_U4(sb + OFF_A1 + hh * 16384 + sw128_off(t, c8)) = pack_bf16x8(x));
+                for (int e = 0; e < 8; ++e) x[e] = -v32[8 * i + e];
+                SM_U4(OFF_A1 + (qq >> 1) * 16384 + sw128_off(t, 4 * (qq & 1) + i)) = pack_bf16x8(x);
             }
         }
         fence_proxy_async();
@@ -551,25 +583,23 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
         wait_mma();
-        // q, k and v of this chunk are consumed: prefetch the next chunk's
+        // q of this chunk is consumed: prefetch the next chunk's
         if (tid == 0 && c + 1 < nchunks) {
             issue_q(t0 + kC);
-            issue_k(t0 + kC);
-            issue_v(t0 + kC);
-            issued[0] = issued[1] = issued[2] = c + 1;
+            issued[0] = c + 1;
         }
 
         // ---------------- step 8: U (D1 rows 0..63) -> bf16 MN-major B operand
         if (sp < 2) {
             const int t = 32 * sp + lane;
-            float v64[64];
-            tmem_ld64(tmem + ((uint32_t)(32 * sp) << 16) + TM_D1 + 64 * hh, v64);
+            float v32[32];
+            tmem_ld32(tlane + TM_D1 + 32 * qq, v32);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int i = 0; i < 4; ++i) {
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = v64[8 * c8 + e];
-                (SM_U4(gr + GR_U + hh * 8192 + sw128_off(t, c8)) = pack_bf16x8(x));
+                for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
+                SM_U4(OFF_GR + GR_U + (qq >> 1) * 8192 + sw128_off(t, 4 * (qq & 1) + i)) = pack_bf16x8(x);
             }
         }
         fence_proxy_async();
@@ -585,47 +615,49 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = sw128_desc(gr + GR_U + kk * 2048, 8192, 1024);
                 mma_bf16(tmem + TM_D1, sw128_desc(gr + GR_P + kk * 32, 0, 1024), bd, id2, 1);
-                mma_bf16(tmem + TM_D3, sw128_desc(sb + OFF_G + kk * 2048, 8192, 1024), bd, id3, kk > 0);
+                mma_bf16(tmem + TM_D3, sw128_desc(sb + kbuf + kk * 2048, 8192, 1024), bd, id3, kk > 0);
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
+        if (tid < kC && c + 1 < nchunks)
+            beta_next = (tid < eos - (t0 + kC)) ? beta[(size_t)(t0 + kC + tid) * H + h] : 0.f;
         wait_mma();
+        // Khat is consumed: the next chunk's v goes into its buffer
         if (tid == 0 && c + 1 < nchunks) {
-            issue_g(t0 + kC);
-            issued[3] = c + 1;
+            issue_v(t0 + kC, kbuf);
+            issued[2] = c + 1;
         }
 
         // ---------------- step 10: outputs and the state update
         {
-            const uint32_t lanebase = tmem + ((uint32_t)(32 * sp) << 16);
             if (sp >= 2) {
                 const int t = 32 * (sp - 2) + lane;
-                float v64[64];
-                tmem_ld64(lanebase + TM_D1 + 64 * hh, v64);
+                float v32[32];
+                tmem_ld32(tlane + TM_D1 + 32 * qq, v32);
                 if (t < lenc) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(t0 + t) * H + h) * kD + 64 * hh);
+                    uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(t0 + t) * H + h) * kD + 32 * qq);
 #pragma unroll
-                    for (int c8 = 0; c8 < 8; ++c8) {
+                    for (int i = 0; i < 4; ++i) {
                         float x[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = v64[8 * c8 + e];
-                        dst[c8] = pack_bf16x8(x);
+                        for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
+                        dst[i] = pack_bf16x8(x);
                     }
                 }
             }
-            const float dec = SM_F(sb + OFF_VEC + VEC_DEC + 4 * srow);
-            {
-                float v64[64];
-                tmem_ld64(lanebase + TM_D3 + 64 * hh, v64);
+            const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * srow);
+            float ds[64];    // [D3 | S]
+            tmem_ld32x2(tlane + TM_D3 + 32 * qq, tlane + TM_S + 32 * qq, ds);
+            float S[32];
 #pragma unroll
-                for (int j = 0; j < 64; ++j) S[j] = dec * S[j] + v64[j];
-            }
+            for (int j = 0; j < 32; ++j) S[j] = dec * ds[32 + j] + ds[j];
+            tmem_st32(tlane + TM_S + 32 * qq, S);
 #pragma unroll
-            for (int c8 = 0; c8 < 8; ++c8) {
+            for (int i = 0; i < 4; ++i) {
                 float x[8];
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = S[8 * c8 + e];
-                (SM_U4(sb + OFF_S + hh * 16384 + sw128_off(srow, c8)) = pack_bf16x8(x));
+                for (int e = 0; e < 8; ++e) x[e] = S[8 * i + e];
+                SM_U4(s_smem + sw128_off(srow, 4 * (qq & 1) + i)) = pack_bf16x8(x);
             }
         }
         fence_proxy_async();
@@ -645,9 +677,12 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     mbar_wait(sb + OFF_BAR + bars[i], issued[i] & 1, 100000000ull);
         }
     } else if (final_state != nullptr) {
-        float *dst = final_state + unit * kD * kD + (size_t)srow * kD + 64 * hh;
+        tc_fence_after();
+        float S[32];
+        tmem_ld32(tlane + TM_S + 32 * qq, S);
+        float *dst = final_state + unit * kD * kD + (size_t)srow * kD + 32 * qq;
 #pragma unroll
-        for (int j = 0; j < 64; j += 4)
+        for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
     tc_fence_before();
@@ -656,6 +691,10 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         tc_fence_after();
         tmem_dealloc(tmem, TM_COLS);
     }
+#undef SM_F
+#undef SM_F4
+#undef SM_U4
+#undef SM_H
 }
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,

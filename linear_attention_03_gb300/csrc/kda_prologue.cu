@@ -6,7 +6,7 @@
 //
 // Kernel 1 (conv_swish_norm): one pass over a raw q, k or v tensor.  Each
 // thread owns 8 consecutive channels of one head (16-byte loads for bf16) and
-// walks a tile of TT tokens, keeping the last three raw inputs of its
+// walks a tile of 256 tokens (loads double-buffered 4 tokens ahead), keeping the last three raw inputs of its
 // channels in registers as the causal window:
 //     y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t     (fp32)
 // History is zero before each document start (cu_seqlens).  Then
@@ -22,8 +22,8 @@ namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kTileTokens = 32;   // tokens per CTA
-constexpr int kBatch = 8;         // tokens loaded ahead per thread
+constexpr int kTileTokens = 256;  // tokens per CTA
+constexpr int kBatch = 4;         // tokens per prefetched batch
 constexpr float kL2Eps = 1e-6f;
 constexpr float kGmin = -5.0f;
 
@@ -45,8 +45,38 @@ __device__ __forceinline__ int64_t clamp_off(const int32_t *cu, int n, int N, in
     return min((int64_t)max(cu[n], 0), T);
 }
 
+// Raw row of 8 channels kept packed until used (bf16: one uint4; fp32: two).
+template <typename Tin> struct Raw8;
+template <> struct Raw8<__nv_bfloat16> {
+    uint4 u;
+    __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
+        u = __ldcs(reinterpret_cast<const uint4 *>(p));
+    }
+    __device__ __forceinline__ void zero() { u = make_uint4(0, 0, 0, 0); }
+    __device__ __forceinline__ void get(float (&x)[8]) const {
+        const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[2 * i] = __uint_as_float(w[i] << 16);
+            x[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+        }
+    }
+};
+template <> struct Raw8<float> {
+    float4 a, b;
+    __device__ __forceinline__ void load(const float *p) {
+        a = __ldcs(reinterpret_cast<const float4 *>(p));
+        b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
+    __device__ __forceinline__ void get(float (&x)[8]) const {
+        x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
+        x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
+    }
+};
+
 template <typename Tin, int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, 2)
 conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
                        const Tin *__restrict__ x2, const float *__restrict__ conv_w,
                        const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
@@ -64,12 +94,15 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
     const int64_t row_stride = (int64_t)H * D;
     const int64_t ch = (int64_t)(live ? h : 0) * D + 8 * sub;   // first channel
 
+    // weights [3, H*D, 4]: the 4 taps of a channel are one float4
     float w[4][8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e)
-#pragma unroll
-        for (int j = 0; j < 4; ++j)
-            w[j][e] = live ? conv_w[((int64_t)which * row_stride + ch + e) * 4 + j] : 0.f;
+    for (int e = 0; e < 8; ++e) {
+        const float4 wv = live ? __ldg(reinterpret_cast<const float4 *>(
+                                     conv_w + ((int64_t)which * row_stride + ch + e) * 4))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[0][e] = wv.x; w[1][e] = wv.y; w[2][e] = wv.z; w[3][e] = wv.w;
+    }
 
     const int64_t t0 = (int64_t)blockIdx.x * kTileTokens;
     const int64_t t1 = min(T, t0 + kTileTokens);
@@ -81,25 +114,22 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const int64_t tj = t0 - 3 + j;
-        if (live && tj >= start && tj >= 0) {
-            Elem<Tin>::load8(x + tj * row_stride + ch, hist[j]);
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
-        }
+        Raw8<Tin> r;
+        if (live && tj >= start && tj >= 0) r.load(x + tj * row_stride + ch); else r.zero();
+        r.get(hist[j]);
     }
 
-    for (int64_t tb = t0; tb < t1; tb += kBatch) {
-        float cur[kBatch][8];
+    // double-buffered batches of kBatch tokens, kept packed until used; the
+    // two slots are compile-time indices so the buffers stay in registers
+    Raw8<Tin> buf0[kBatch], buf1[kBatch];
+    auto fetch = [&](Raw8<Tin>(&bufr)[kBatch], int64_t tb) {
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
-            if (live && tb + b < t1) {
-                Elem<Tin>::load8(x + (tb + b) * row_stride + ch, cur[b]);
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) cur[b][e] = 0.f;
-            }
+            if (live && tb + b < t1) bufr[b].load(x + (tb + b) * row_stride + ch);
+            else bufr[b].zero();
         }
+    };
+    auto process = [&](const Raw8<Tin>(&bufr)[kBatch], int64_t tb) {
 #pragma unroll
         for (int b = 0; b < kBatch; ++b) {
             const int64_t t = tb + b;
@@ -113,17 +143,19 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
 #pragma unroll
                     for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
             }
+            float cur[8];
+            bufr[b].get(cur);
             float s[8];
             float ss = 0.f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) {
                 const float yv = w[0][e] * hist[0][e] + w[1][e] * hist[1][e] +
-                                 w[2][e] * hist[2][e] + w[3][e] * cur[b][e];
+                                 w[2][e] * hist[2][e] + w[3][e] * cur[e];
                 s[e] = yv / (1.f + __expf(-yv));
                 ss += s[e] * s[e];
                 hist[0][e] = hist[1][e];
                 hist[1][e] = hist[2][e];
-                hist[2][e] = cur[b][e];
+                hist[2][e] = cur[e];
             }
             if (normalise) {
 #pragma unroll
@@ -134,6 +166,14 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
             }
             if (live) Elem<Tin>::store8(y + t * row_stride + ch, s);
         }
+    };
+    fetch(buf0, t0);
+    for (int64_t tb = t0; tb < t1; tb += 2 * kBatch) {
+        if (tb + kBatch < t1) fetch(buf1, tb + kBatch);
+        process(buf0, tb);
+        if (tb + kBatch >= t1) break;
+        if (tb + 2 * kBatch < t1) fetch(buf0, tb + 2 * kBatch);
+        process(buf1, tb + kBatch);
     }
 }
 
