@@ -331,6 +331,70 @@ def bench_long(kda, dist, args, peaks):
                                              peaks["hbm_gbs"], traffic_for("chunk_kernel", T))}}
 
 
+# per (sequence, head): state read + written, raw q/k/v, conv cache read +
+# written (3 taps x 3 tensors), z_g, z_beta, out
+CONV_DECODE_BYTES = 2 * D * D * 4 + 3 * D * 2 + 2 * 9 * D * 2 + D * 4 + 4 + D * 2
+# per (sequence, head) for K drafts: state_in read, state_out written, and
+# per draft q,k,v (bf16), g, beta, out
+def verify_bytes(K):
+    return 2 * D * D * 4 + K * (3 * D * 2 + D * 4 + 4 + D * 2)
+# per (token, head): o and z read, y written (bf16)
+GATE_BYTES = 3 * D * 2
+
+
+def bench_extras(kda, dist, args, peaks):
+    """The rows beyond the core path, each timed on its own."""
+    gen = torch.Generator(device="cuda").manual_seed(11)
+    rnd = lambda *s, dt=torch.float32, sc=1.0: (sc * torch.randn(*s, generator=gen, device="cuda")).to(dt)
+    res = {}
+    N = 256
+    # decode with the ShortConv cache: 256 sequences x 1 token
+    raw = [rnd(N, H, D, dt=torch.bfloat16) for _ in range(3)]
+    conv_w = rnd(3, H * D, 4, sc=0.5)
+    cache = rnd(N, 3, 3, H, D, dt=torch.bfloat16)
+    z_g, z_b = rnd(N, H, D), rnd(N, H)
+    state = rnd(N, H, D, D, sc=0.01)
+    out = torch.empty_like(raw[0])
+    step = lambda: kda.kda_decode_step_conv(raw[0], raw[1], raw[2], conv_w, cache, z_g, z_b, state,
+                                            out=out)
+    total, per = time_steps(dist, step, args.steps, args.warmup)
+    res["decode_conv"] = {"workload": "decode with the ShortConv cache: 256 sequences x 1 token",
+                          "value": round(args.steps / (total * 1e-3), 2), "unit": "steps/s",
+                          "roofline": roofline(CONV_DECODE_BYTES * N * H, statistics.mean(per),
+                                               peaks["hbm_gbs"])}
+    del cache, raw
+    # verify: 256 sequences x 4 drafts from a read-only state, accept 2
+    K = 4
+    q = torch.nn.functional.normalize(rnd(N * K, H, D), dim=-1).to(torch.bfloat16)
+    k = torch.nn.functional.normalize(rnd(N * K, H, D), dim=-1).to(torch.bfloat16)
+    v = rnd(N * K, H, D, dt=torch.bfloat16)
+    g = -5.0 * torch.sigmoid(rnd(N * K, H, D))
+    b = torch.sigmoid(rnd(N * K, H))
+    acc = torch.full((N,), 2, dtype=torch.int32, device="cuda")
+    s_out = torch.empty_like(state)
+    o2 = torch.empty_like(v)
+    step = lambda: kda.kda_decode_verify(q, k, v, g, b, state, acc, K, out=o2, state_out=s_out)
+    total, per = time_steps(dist, step, args.steps, args.warmup)
+    res["verify"] = {"workload": "verify: 256 sequences x 4 drafts, rollback state after 2",
+                     "value": round(args.steps / (total * 1e-3), 2), "unit": "verifies/s",
+                     "roofline": roofline(verify_bytes(K) * N * H, statistics.mean(per),
+                                          peaks["hbm_gbs"])}
+    del q, k, v, g, b, state, s_out, o2
+    # output gate on the T=4096 shape
+    T = 4096
+    o = rnd(T, H, D, dt=torch.bfloat16)
+    z = rnd(T, H, D, dt=torch.bfloat16)
+    w = torch.rand(D, device="cuda") + 0.5
+    y = torch.empty_like(o)
+    step = lambda: kda.kda_output_gate(o, z, w, out=y)
+    total, per = time_steps(dist, step, args.steps, args.warmup)
+    res["output_gate"] = {"workload": "head RMSNorm x sigmoid(gate), T=4096, H=96, d=128 bf16",
+                          "value": round(T * args.steps / (total * 1e-3), 1), "unit": "tokens/s",
+                          "roofline": roofline(GATE_BYTES * T * H, statistics.mean(per),
+                                               peaks["hbm_gbs"])}
+    return res
+
+
 def cpu_baseline(synth, heads):
     """fp64 oracle on the host cores over `heads` of the T=4096 workload."""
     import oracle
@@ -392,7 +456,7 @@ def main():
     ap.add_argument("--no-decode", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     # smaller cases for profiler captures (the printed line then describes them)
-    ap.add_argument("--only", choices=["prefill", "decode", "long"])
+    ap.add_argument("--only", choices=["prefill", "decode", "long", "extras"])
     ap.add_argument("--prefill-tokens", type=int, default=0)
     ap.add_argument("--decode-seqs", type=int, default=0)
     args = ap.parse_args()
@@ -411,7 +475,8 @@ def main():
     if args.only:
         run = {"prefill": lambda: bench_prefill(kda, synth, dist, args, peaks),
                "decode": lambda: bench_decode(kda, synth, dist, args, peaks),
-               "long": lambda: bench_long(kda, dist, args, peaks)}[args.only]
+               "long": lambda: bench_long(kda, dist, args, peaks),
+               "extras": lambda: bench_extras(kda, dist, args, peaks)}[args.only]
         res = run()
         if dist.rank == 0:
             print(json.dumps({"only": args.only, "result": res}), flush=True)
@@ -423,6 +488,8 @@ def main():
     dec = None if args.no_decode else bench_decode(kda, synth, dist, args, peaks)
     torch.cuda.empty_cache()
     lng = None if args.no_long else bench_long(kda, dist, args, peaks)
+    torch.cuda.empty_cache()
+    ext = bench_extras(kda, dist, args, peaks)
     clk = clocks.stop()
     cb = None
     if dist.rank == 0 and not args.no_cpu_baseline:
@@ -435,7 +502,7 @@ def main():
             "ms_per_step": round(pre["total_ms"] / args.steps, 4),
             "roofline": dict(pre["roofline"], peak_source=f"{peaks['source']} HBM copy"),
             "cpu_baseline": cb, "e2e": pre["e2e"], "gpu_launches": pre["gpu_launches"],
-            "clocks": clk, "decode": dec, "long_context": lng})
+            "clocks": clk, "decode": dec, "long_context": lng, "extras": ext})
         print(json.dumps(line), flush=True)
     dist.close()
     return 0

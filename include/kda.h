@@ -156,6 +156,54 @@ KDA_API kda_status kda_prologue(const void *q_raw, const void *k_raw,
                         float *beta, void *stream);
 
 /*
+ * One decode step with the ShortConv cache ("From GPT-2 to Kimi K3",
+ * Chapter 5: the width-4 convolution "is a short local preprocessor whose
+ * state must also be cached during decoding").  Per sequence and head: the
+ * prologue of kda_prologue (conv over the cached window, Swish, L2 norm of
+ * q and k, the two gates) on this token's raw projections, then the update
+ * of kda_decode_step, in one kernel.
+ *   q_raw, k_raw, v_raw [N, H, d] qkv_dtype (this token's raw projections)
+ *   conv_w [3, H*d, 4] fp32 (as kda_prologue)
+ *   conv_state [N, 3, 3, H, d] qkv_dtype: the raw inputs of the previous three
+ *       tokens (index 0 = t-3 ... 2 = t-1; then q, k, v), zero for a new
+ *       sequence; shifted in place (this token becomes index 2)
+ *   z_g [N, H, d] fp32, z_beta [N, H] fp32 (gate logits)
+ *   state [N, H, d, d] fp32 in place;  out [N, H, d] qkv_dtype
+ * Equivalent to kda_prologue + kda_prefill over each sequence's whole history.
+ */
+KDA_API kda_status kda_decode_step_conv(const void *q_raw, const void *k_raw, const void *v_raw,
+                                        const float *conv_w, void *conv_state, const float *z_g,
+                                        const float *z_beta, float *state, void *out,
+                                        int32_t N, kda_dims dims, void *stream);
+
+/*
+ * Multi-token verify with a rollback point, for speculative decoding ("From
+ * GPT-2 to Kimi K3", Chapter 14: accepted draft updates are replayed on
+ * chip; cached KDA states are read-only snapshots and a hit works on a
+ * private copy).  Each of N sequences runs its K draft tokens from
+ * state_in, which is not modified; every draft output is written, and
+ * state_out receives the state after the first accept[n] tokens.
+ *   q, k, g [N*K, H, d] (row n*K + t is draft t of sequence n); v, out
+ *   likewise; beta [N*K, H]; state_in, state_out [N, H, d, d] fp32 (must not
+ *   alias); accept [N] int32 device, clamped to 0..K.
+ */
+KDA_API kda_status kda_decode_verify(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, const float *state_in,
+                                     const int32_t *accept, int32_t N, int32_t K, kda_dims dims,
+                                     void *out, float *state_out, void *stream);
+
+/*
+ * Head-wise RMSNorm and the full-rank output gate that follow the
+ * recurrent read ("From GPT-2 to Kimi K3", Chapter 5 "A third gate: control
+ * what leaves the module"; infra diagram KDA card "Head RMSNorm + gate"):
+ *   y = o / sqrt(mean over the head's d channels of o^2 + eps) * w * sigmoid(z)
+ *   o, z, y [T, H, d] qkv_dtype (z = the gate logits W_g x);  w [d] fp32 or
+ *   NULL (ones), shared by all heads.  y may alias o.
+ */
+KDA_API kda_status kda_output_gate(const void *o, const void *z, const float *weight, int64_t T,
+                                   kda_dims dims, float eps, void *y, void *stream);
+
+/*
  * Waits for `stream`, then copies the workspace status word (one of the
  * KDA_DEVICE_* values) to *status_out.  Returns KDA_ERR_DEVICE /
  * KDA_ERR_TIMEOUT when the word is set, KDA_OK when it is clear.

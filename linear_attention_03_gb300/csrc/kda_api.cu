@@ -192,6 +192,76 @@ kda_status kda_prologue(const void *q_raw, const void *k_raw,
     return KDA_OK;
 }
 
+kda_status kda_decode_step_conv(const void *q_raw, const void *k_raw, const void *v_raw,
+                                const float *conv_w, void *conv_state, const float *z_g,
+                                const float *z_beta, float *state, void *out, int32_t N,
+                                kda_dims dims, void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (N < 0) return fail(KDA_ERR_INVALID, "N must be >= 0%s");
+    if ((int64_t)N * dims.H > INT32_MAX) return fail(KDA_ERR_INVALID, "N * H too large%s");
+    if (N == 0) return KDA_OK;
+    KDA_TRY(need(q_raw, "q_raw"));
+    KDA_TRY(need(k_raw, "k_raw"));
+    KDA_TRY(need(v_raw, "v_raw"));
+    KDA_TRY(need(conv_w, "conv_w"));
+    KDA_TRY(need(conv_state, "conv_state"));
+    KDA_TRY(need(z_g, "z_g"));
+    KDA_TRY(need4(z_beta, "z_beta"));
+    KDA_TRY(need(state, "state"));
+    KDA_TRY(need(out, "out"));
+    cudaError_t err = kda::launch_decode_conv(q_raw, k_raw, v_raw, conv_w, conv_state, z_g, z_beta,
+                                              state, out, N, dims.H, dims.d_k,
+                                              (kda_dtype)dims.qkv_dtype,
+                                              static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "decode-with-conv launch");
+    return KDA_OK;
+}
+
+kda_status kda_decode_verify(const void *q, const void *k, const void *v, const float *g,
+                             const float *beta, const float *state_in, const int32_t *accept,
+                             int32_t N, int32_t K, kda_dims dims, void *out, float *state_out,
+                             void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (N < 0 || K < 1) return fail(KDA_ERR_INVALID, "N must be >= 0 and K >= 1%s");
+    if ((int64_t)N * K * dims.H > INT32_MAX) return fail(KDA_ERR_INVALID, "N * K * H too large%s");
+    if (N == 0) return KDA_OK;
+    KDA_TRY(need(q, "q"));
+    KDA_TRY(need(k, "k"));
+    KDA_TRY(need(v, "v"));
+    KDA_TRY(need(g, "g"));
+    KDA_TRY(need4(beta, "beta"));
+    KDA_TRY(need(state_in, "state_in"));
+    KDA_TRY(need4(accept, "accept"));
+    KDA_TRY(need(out, "out"));
+    KDA_TRY(need(state_out, "state_out"));
+    if (state_in == state_out) return fail(KDA_ERR_INVALID, "state_out must not alias state_in%s");
+    cudaError_t err = kda::launch_verify(q, k, v, g, beta, state_in, accept, N, K, dims.H,
+                                         dims.d_k, (kda_dtype)dims.qkv_dtype, out, state_out,
+                                         static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "verify launch");
+    return KDA_OK;
+}
+
+kda_status kda_output_gate(const void *o, const void *z, const float *weight, int64_t T,
+                           kda_dims dims, float eps, void *y, void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (T < 0) return fail(KDA_ERR_INVALID, "T must be >= 0%s");
+    if (!(eps >= 0.f)) return fail(KDA_ERR_INVALID, "eps must be >= 0%s");
+    if (T == 0) return KDA_OK;
+    KDA_TRY(need(o, "o"));
+    KDA_TRY(need(z, "z"));
+    KDA_TRY(maybe(weight, "weight"));
+    KDA_TRY(need(y, "y"));
+    cudaError_t err = kda::launch_output_gate(o, z, weight, T * dims.H, dims.d_k,
+                                              (kda_dtype)dims.qkv_dtype, eps, y,
+                                              static_cast<cudaStream_t>(stream));
+    if (err != cudaSuccess) return cuda_fail(err, "output gate launch");
+    return KDA_OK;
+}
+
 kda_status kda_get_device_status(const void *workspace, int32_t *status_out,
                                  void *stream) {
     g_last_error[0] = '\0';

@@ -121,6 +121,244 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
     }
 }
 
+// ---------------------------------------------------------------------------
+// Shared pieces of the one-pass update used by the decode-with-conv and the
+// multi-token verify kernels: the per-thread state tile is 16 rows x 4
+// columns (D = 128) held as float4, the column reductions over the old state
+// go through shared memory, and the update is written back in registers.
+
+template <int D>
+struct TokenSmem {
+    float ka[D];      // alpha_i k_i
+    float qa[D];      // alpha_i q_i
+    float alpha[D];
+    float k[D];
+    float v[D];
+    float red[24];    // per-warp partial sums (k.q and the L2 norms)
+    float kq, beta;
+};
+
+// Given a staged token (sm), produce o (written by row group 0) and update
+// the register tile s in place.
+template <typename Tin, int D>
+__device__ __forceinline__ void token_update(float4 (&s)[DecodeCfg<Tin, D>::ROWS],
+                                             const TokenSmem<D> &sm,
+                                             float4 (&part)[2][DecodeCfg<Tin, D>::RG]
+                                                           [DecodeCfg<Tin, D>::COLG],
+                                             int r, int c, Tin *out_vec) {
+    using C = DecodeCfg<Tin, D>;
+    float4 pa = make_float4(0.f, 0.f, 0.f, 0.f), pb = pa;
+#pragma unroll
+    for (int i = 0; i < C::ROWS; ++i) {
+        const int row = r * C::ROWS + i;
+        const float ka = sm.ka[row], qa = sm.qa[row];
+        pa.x += ka * s[i].x; pa.y += ka * s[i].y; pa.z += ka * s[i].z; pa.w += ka * s[i].w;
+        pb.x += qa * s[i].x; pb.y += qa * s[i].y; pb.z += qa * s[i].z; pb.w += qa * s[i].w;
+    }
+    part[0][r][c] = pa;
+    part[1][r][c] = pb;
+    __syncthreads();
+    float4 a4 = make_float4(0.f, 0.f, 0.f, 0.f), b4 = a4;
+#pragma unroll
+    for (int j = 0; j < C::RG; ++j) {
+        const float4 x = part[0][j][c], y = part[1][j][c];
+        a4.x += x.x; a4.y += x.y; a4.z += x.z; a4.w += x.w;
+        b4.x += y.x; b4.y += y.y; b4.z += y.z; b4.w += y.w;
+    }
+    const float bt = sm.beta, kq = sm.kq;
+    float4 u;
+    u.x = bt * (sm.v[4 * c + 0] - a4.x); u.y = bt * (sm.v[4 * c + 1] - a4.y);
+    u.z = bt * (sm.v[4 * c + 2] - a4.z); u.w = bt * (sm.v[4 * c + 3] - a4.w);
+    if (r == 0) {
+        Elem<Tin>::store(out_vec + 4 * c + 0, b4.x + u.x * kq);
+        Elem<Tin>::store(out_vec + 4 * c + 1, b4.y + u.y * kq);
+        Elem<Tin>::store(out_vec + 4 * c + 2, b4.z + u.z * kq);
+        Elem<Tin>::store(out_vec + 4 * c + 3, b4.w + u.w * kq);
+    }
+#pragma unroll
+    for (int i = 0; i < C::ROWS; ++i) {
+        const int row = r * C::ROWS + i;
+        const float a = sm.alpha[row], ki = sm.k[row];
+        s[i].x = a * s[i].x + ki * u.x; s[i].y = a * s[i].y + ki * u.y;
+        s[i].z = a * s[i].z + ki * u.z; s[i].w = a * s[i].w + ki * u.w;
+    }
+}
+
+// Block-wide sums of three values per thread in one pass (all threads call it).
+template <int THREADS>
+__device__ __forceinline__ float3 block_sum3(float3 x, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        x.x += __shfl_xor_sync(0xffffffffu, x.x, o);
+        x.y += __shfl_xor_sync(0xffffffffu, x.y, o);
+        x.z += __shfl_xor_sync(0xffffffffu, x.z, o);
+    }
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) {
+        red[3 * (threadIdx.x >> 5)] = x.x;
+        red[3 * (threadIdx.x >> 5) + 1] = x.y;
+        red[3 * (threadIdx.x >> 5) + 2] = x.z;
+    }
+    __syncthreads();
+    float3 t = make_float3(0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) {
+        t.x += red[3 * w]; t.y += red[3 * w + 1]; t.z += red[3 * w + 2];
+    }
+    return t;
+}
+
+// Block-wide sum of one value per thread (all threads call it).
+template <int THREADS>
+__device__ __forceinline__ float block_sum(float x, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = x;
+    __syncthreads();
+    float t = 0.f;
+#pragma unroll
+    for (int w = 0; w < THREADS / 32; ++w) t += red[w];
+    return t;
+}
+
+// One decode step with the ShortConv cache ("From GPT-2 to Kimi K3",
+// Chapter 5: the short convolution "is a short local preprocessor whose
+// state must also be cached during decoding").  The prologue of the
+// infra diagram's KDA card runs on the token's raw projections against the
+// cached last three raw inputs, then the same one-pass update as
+// decode_kernel.  conv_state [N, 3 taps (t-3, t-2, t-1), 3 (q,k,v), H, D] in
+// the raw dtype is shifted in place.
+template <typename Tin, int D>
+__global__ void __launch_bounds__(DecodeCfg<Tin, D>::THREADS)
+decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
+                   const Tin *__restrict__ v_raw, const float *__restrict__ conv_w,
+                   Tin *__restrict__ conv_state, const float *__restrict__ z_g,
+                   const float *__restrict__ z_beta, float *__restrict__ state,
+                   Tin *__restrict__ out, int32_t H) {
+    using C = DecodeCfg<Tin, D>;
+    const int unit = blockIdx.x;             // sequence * H + head
+    const int n = unit / H, h = unit % H;
+    const int tid = threadIdx.x;
+    const int c = tid % C::COLG, r = tid / C::COLG;
+    __shared__ TokenSmem<D> sm;
+    __shared__ float4 s_part[2][C::RG][C::COLG];
+
+    float *S = state + (size_t)unit * D * D;
+    float4 s[C::ROWS];
+#pragma unroll
+    for (int i = 0; i < C::ROWS; ++i)
+        s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(r * C::ROWS + i) * D) + c);
+
+    // prologue for channel ch = tid (tid < D): conv over the cached window
+    const size_t vec = (size_t)unit * D;
+    const int64_t HD = (int64_t)H * D;
+    float yq = 0.f, yk = 0.f, yv = 0.f;
+    if (tid < D) {
+        const int ch = tid;
+        float y3[3];
+        const Tin *raws[3] = {q_raw, k_raw, v_raw};
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            const float4 w = __ldg(reinterpret_cast<const float4 *>(
+                conv_w + ((int64_t)i * HD + (int64_t)h * D + ch) * 4));
+            Tin *cs = conv_state + ((size_t)n * 9 + i) * HD + (size_t)h * D + ch;  // tap 0
+            const Tin h0 = cs[0], h1 = cs[3 * HD], h2 = cs[6 * HD];
+            const Tin x = raws[i][vec + ch];
+            const float yv2 = w.x * Elem<Tin>::load(&h0) + w.y * Elem<Tin>::load(&h1) +
+                              w.z * Elem<Tin>::load(&h2) + w.w * Elem<Tin>::load(&x);
+            y3[i] = __fdividef(yv2, 1.f + __expf(-yv2));
+            cs[0] = h1;                      // shift the window: t-2 -> t-3, ...
+            cs[3 * HD] = h2;
+            cs[6 * HD] = x;
+        }
+        yq = y3[0]; yk = y3[1]; yv = y3[2];
+    }
+    // |q|^2, |k|^2 and q.k of the unnormalised head vectors in one pass;
+    // k.q of the normalised vectors is then iq * ik * (q.k)
+    const float3 sums = block_sum3<C::THREADS>(make_float3(yq * yq, yk * yk, yq * yk), sm.red);
+    const float iq = rsqrtf(sums.x + 1e-6f), ik = rsqrtf(sums.y + 1e-6f);
+    const float kq = iq * ik * sums.z;
+    if (tid < D) {
+        const float qq = yq * iq, kk = yk * ik;
+        const float a = __expf(-5.f / (1.f + __expf(-z_g[vec + tid])));
+        sm.alpha[tid] = a;
+        sm.k[tid] = kk;
+        sm.ka[tid] = a * kk;
+        sm.qa[tid] = a * qq;
+        sm.v[tid] = yv;
+    }
+    if (tid == 0) {
+        sm.kq = kq;
+        sm.beta = 1.f / (1.f + __expf(-z_beta[unit]));
+    }
+    __syncthreads();
+    token_update<Tin, D>(s, sm, s_part, r, c, out + vec);
+#pragma unroll
+    for (int i = 0; i < C::ROWS; ++i)
+        __stcs(reinterpret_cast<float4 *>(S + (size_t)(r * C::ROWS + i) * D) + c, s[i]);
+}
+
+// Multi-token verify with a rollback point: K draft tokens of one sequence
+// run from a read-only state (the snapshot semantics of "From GPT-2 to Kimi
+// K3", Chapter 14: cached KDA states are read-only, a hit works on a private
+// copy); every draft token's output is written and state_out receives the
+// state after the first accept[n] tokens (the accepted prefix).
+template <typename Tin, int D>
+__global__ void __launch_bounds__(DecodeCfg<Tin, D>::THREADS)
+verify_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+              const float *__restrict__ g, const float *__restrict__ beta,
+              const float *__restrict__ state_in, const int32_t *__restrict__ accept,
+              int32_t K, int32_t H, Tin *__restrict__ out, float *__restrict__ state_out) {
+    using C = DecodeCfg<Tin, D>;
+    const int unit = blockIdx.x;             // sequence * H + head
+    const int n = unit / H, h = unit % H;
+    const int tid = threadIdx.x;
+    const int c = tid % C::COLG, r = tid / C::COLG;
+    __shared__ TokenSmem<D> sm;
+    __shared__ float4 s_part[2][C::RG][C::COLG];
+
+    const float *S0 = state_in + (size_t)unit * D * D;
+    float *S1 = state_out + (size_t)unit * D * D;
+    float4 s[C::ROWS];
+#pragma unroll
+    for (int i = 0; i < C::ROWS; ++i)
+        s[i] = __ldcs(reinterpret_cast<const float4 *>(S0 + (size_t)(r * C::ROWS + i) * D) + c);
+    int acc = accept[n];
+    acc = acc < 0 ? 0 : (acc > K ? K : acc);
+
+    auto store_state = [&]() {
+#pragma unroll
+        for (int i = 0; i < C::ROWS; ++i)
+            __stcs(reinterpret_cast<float4 *>(S1 + (size_t)(r * C::ROWS + i) * D) + c, s[i]);
+    };
+    for (int t = 0; t < K; ++t) {
+        if (t == acc) store_state();
+        const size_t vec = ((size_t)(n * K + t) * H + h) * D;
+        float kqp = 0.f;
+        if (tid < D) {
+            const float ki = Elem<Tin>::load(k + vec + tid);
+            const float qi = Elem<Tin>::load(q + vec + tid);
+            const float a = __expf(g[vec + tid]);
+            sm.alpha[tid] = a;
+            sm.k[tid] = ki;
+            sm.ka[tid] = a * ki;
+            sm.qa[tid] = a * qi;
+            sm.v[tid] = Elem<Tin>::load(v + vec + tid);
+            kqp = ki * qi;
+        }
+        const float kq = block_sum<C::THREADS>(kqp, sm.red);
+        if (tid == 0) {
+            sm.kq = kq;
+            sm.beta = beta[(size_t)(n * K + t) * H + h];
+        }
+        __syncthreads();
+        token_update<Tin, D>(s, sm, s_part, r, c, out + vec);
+        __syncthreads();   // the next token restages the shared inputs
+    }
+    if (acc == K) store_state();
+}
+
 template <typename Tin, int D>
 cudaError_t run(const void *q, const void *k, const void *v, const float *g,
                 const float *beta, float *state, void *out, int32_t N, int32_t H,
@@ -147,7 +385,66 @@ cudaError_t run_d(const void *q, const void *k, const void *v, const float *g,
     }
 }
 
+template <typename Tin, int D>
+cudaError_t run_conv(const void *q_raw, const void *k_raw, const void *v_raw, const float *conv_w,
+                     void *conv_state, const float *z_g, const float *z_beta, float *state,
+                     void *out, int32_t N, int32_t H, cudaStream_t stream) {
+    const unsigned units = (unsigned)N * (unsigned)H;
+    if (units == 0) return cudaSuccess;
+    decode_conv_kernel<Tin, D><<<units, DecodeCfg<Tin, D>::THREADS, 0, stream>>>(
+        static_cast<const Tin *>(q_raw), static_cast<const Tin *>(k_raw),
+        static_cast<const Tin *>(v_raw), conv_w, static_cast<Tin *>(conv_state), z_g, z_beta,
+        state, static_cast<Tin *>(out), H);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+template <typename Tin, int D>
+cudaError_t run_verify(const void *q, const void *k, const void *v, const float *g,
+                       const float *beta, const float *state_in, const int32_t *accept,
+                       int32_t N, int32_t K, int32_t H, void *out, float *state_out,
+                       cudaStream_t stream) {
+    const unsigned units = (unsigned)N * (unsigned)H;
+    if (units == 0) return cudaSuccess;
+    verify_kernel<Tin, D><<<units, DecodeCfg<Tin, D>::THREADS, 0, stream>>>(
+        static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v), g,
+        beta, state_in, accept, K, H, static_cast<Tin *>(out), state_out);
+    count_launches(1);
+    return cudaGetLastError();
+}
+
+#define KDA_DISPATCH_D(D, CALL)                   \
+    switch (D) {                                  \
+    case 16: { constexpr int DD = 16; return CALL; }   \
+    case 32: { constexpr int DD = 32; return CALL; }   \
+    case 64: { constexpr int DD = 64; return CALL; }   \
+    case 128: { constexpr int DD = 128; return CALL; } \
+    default: return cudaErrorInvalidValue;        \
+    }
+
 }  // namespace
+
+cudaError_t launch_decode_conv(const void *q_raw, const void *k_raw, const void *v_raw,
+                               const float *conv_w, void *conv_state, const float *z_g,
+                               const float *z_beta, float *state, void *out, int32_t N,
+                               int32_t H, int32_t D, kda_dtype dt, cudaStream_t stream) {
+    if (dt == KDA_BF16)
+        KDA_DISPATCH_D(D, (run_conv<__nv_bfloat16, DD>(q_raw, k_raw, v_raw, conv_w, conv_state,
+                                                       z_g, z_beta, state, out, N, H, stream)))
+    KDA_DISPATCH_D(D, (run_conv<float, DD>(q_raw, k_raw, v_raw, conv_w, conv_state, z_g, z_beta,
+                                           state, out, N, H, stream)))
+}
+
+cudaError_t launch_verify(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *state_in, const int32_t *accept,
+                          int32_t N, int32_t K, int32_t H, int32_t D, kda_dtype dt, void *out,
+                          float *state_out, cudaStream_t stream) {
+    if (dt == KDA_BF16)
+        KDA_DISPATCH_D(D, (run_verify<__nv_bfloat16, DD>(q, k, v, g, beta, state_in, accept, N, K,
+                                                         H, out, state_out, stream)))
+    KDA_DISPATCH_D(D, (run_verify<float, DD>(q, k, v, g, beta, state_in, accept, N, K, H, out,
+                                             state_out, stream)))
+}
 
 cudaError_t launch_decode(const void *q, const void *k, const void *v,
                           const float *g, const float *beta, float *state,

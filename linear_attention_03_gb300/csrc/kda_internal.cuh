@@ -109,6 +109,19 @@ cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      float *final_state, int32_t *status,
                                      cudaStream_t stream);
 
+cudaError_t launch_decode_conv(const void *q_raw, const void *k_raw, const void *v_raw,
+                               const float *conv_w, void *conv_state, const float *z_g,
+                               const float *z_beta, float *state, void *out, int32_t N,
+                               int32_t H, int32_t D, kda_dtype dt, cudaStream_t stream);
+
+cudaError_t launch_verify(const void *q, const void *k, const void *v, const float *g,
+                          const float *beta, const float *state_in, const int32_t *accept,
+                          int32_t N, int32_t K, int32_t H, int32_t D, kda_dtype dt, void *out,
+                          float *state_out, cudaStream_t stream);
+
+cudaError_t launch_output_gate(const void *o, const void *z, const float *weight, int64_t rows,
+                               int32_t D, kda_dtype dt, float eps, void *y, cudaStream_t stream);
+
 // Tensor-core chunked prefill (d = 128, bf16 q/k/v).
 bool chunk_prefill_supported(int32_t D, kda_dtype dt);
 cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, const float *g,

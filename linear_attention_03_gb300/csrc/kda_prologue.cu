@@ -151,7 +151,7 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
             for (int e = 0; e < 8; ++e) {
                 const float yv = w[0][e] * hist[0][e] + w[1][e] * hist[1][e] +
                                  w[2][e] * hist[2][e] + w[3][e] * cur[e];
-                s[e] = yv / (1.f + __expf(-yv));
+                s[e] = __fdividef(yv, 1.f + __expf(-yv));
                 ss += s[e] * s[e];
                 hist[0][e] = hist[1][e];
                 hist[1][e] = hist[2][e];

@@ -27,7 +27,8 @@ KDA_F32, KDA_BF16 = 0, 1
 KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT = 0, 1, 2
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
            "kda_prologue", "kda_get_device_status", "kda_last_error",
-           "kda_kernel_launches")
+           "kda_kernel_launches", "kda_decode_step_conv", "kda_decode_verify",
+           "kda_output_gate", "kda_prefill_noalloc")
 
 
 class kda_dims(ctypes.Structure):
@@ -44,11 +45,15 @@ lib.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
 lib.kda_prologue.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
                              _P, _P, _P]
 lib.kda_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+lib.kda_decode_step_conv.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
+lib.kda_decode_verify.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i32, kda_dims, _P, _P, _P]
+lib.kda_output_gate.argtypes = [_P, _P, _P, _i64, kda_dims, ctypes.c_float, _P, _P]
 lib.kda_last_error.argtypes = []
 lib.kda_last_error.restype = ctypes.c_char_p
 lib.kda_kernel_launches.argtypes = []
 lib.kda_kernel_launches.restype = ctypes.c_uint64
-for _fn in (lib.kda_prefill, lib.kda_decode_step, lib.kda_prologue, lib.kda_get_device_status):
+for _fn in (lib.kda_prefill, lib.kda_decode_step, lib.kda_prologue, lib.kda_get_device_status,
+            lib.kda_decode_step_conv, lib.kda_decode_verify, lib.kda_output_gate):
     _fn.restype = ctypes.c_int
 
 
@@ -185,6 +190,75 @@ def kda_prologue(q_raw, k_raw, v_raw, conv_w, z_g=None, z_beta=None, cu_seqlens=
     if st != KDA_OK:
         raise KDAError(st, "kda_prologue")
     return q, k, v, g, beta
+
+
+def kda_decode_step_conv(q_raw, k_raw, v_raw, conv_w, conv_state, z_g, z_beta, state,
+                         out=None):
+    """One decode step through the fused prologue with the ShortConv cache.
+
+    conv_state [N, 3, 3, H, d] (raw dtype) and state [N, H, d, d] are updated
+    in place; returns out [N, H, d]."""
+    N, H, d = q_raw.shape
+    _dev(q_raw, "q_raw")
+    _dev(k_raw, "k_raw", q_raw.dtype, q_raw.shape)
+    _dev(v_raw, "v_raw", q_raw.dtype, q_raw.shape)
+    _dev(conv_w, "conv_w", torch.float32, (3, H * d, 4))
+    _dev(conv_state, "conv_state", q_raw.dtype, (N, 3, 3, H, d))
+    _dev(z_g, "z_g", torch.float32, q_raw.shape)
+    _dev(z_beta, "z_beta", torch.float32, (N, H))
+    _dev(state, "state", torch.float32, (N, H, d, d))
+    if out is None:
+        out = torch.empty_like(v_raw)
+    _dev(out, "out", q_raw.dtype, q_raw.shape)
+    st = lib.kda_decode_step_conv(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w),
+                                  _ptr(conv_state), _ptr(z_g), _ptr(z_beta), _ptr(state),
+                                  _ptr(out), N, dims_of(q_raw), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_step_conv")
+    return out
+
+
+def kda_decode_verify(q, k, v, g, beta, state_in, accept, K, out=None, state_out=None):
+    """K draft tokens per sequence from read-only state_in; returns
+    (out [N*K, H, d], state_out [N, H, d, d] = state after accept[n] tokens)."""
+    NK, H, d = q.shape
+    N = NK // K
+    if N * K != NK:
+        raise ValueError("q must hold N*K rows")
+    _dev(q, "q")
+    _dev(k, "k", q.dtype, q.shape)
+    _dev(v, "v", q.dtype, q.shape)
+    _dev(g, "g", torch.float32, q.shape)
+    _dev(beta, "beta", torch.float32, (NK, H))
+    _dev(state_in, "state_in", torch.float32, (N, H, d, d))
+    acc = accept if (isinstance(accept, torch.Tensor) and accept.is_cuda) else \
+        torch.as_tensor(accept, dtype=torch.int32).to(q.device)
+    _dev(acc, "accept", torch.int32, (N,))
+    if out is None:
+        out = torch.empty_like(v)
+    if state_out is None:
+        state_out = torch.empty_like(state_in)
+    st = lib.kda_decode_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
+                               _ptr(acc), N, K, dims_of(q), _ptr(out), _ptr(state_out),
+                               _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_decode_verify")
+    return out, state_out
+
+
+def kda_output_gate(o, z, weight=None, eps=1e-6, out=None):
+    """Head RMSNorm x sigmoid(gate logits); o, z [T, H, d]; weight [d] or None."""
+    T, H, d = o.shape
+    _dev(o, "o")
+    _dev(z, "z", o.dtype, o.shape)
+    _dev(weight, "weight", torch.float32, (d,))
+    if out is None:
+        out = torch.empty_like(o)
+    st = lib.kda_output_gate(_ptr(o), _ptr(z), _ptr(weight), T, dims_of(o), float(eps),
+                             _ptr(out), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_output_gate")
+    return out
 
 
 def kda_get_device_status(workspace) -> int:

@@ -37,6 +37,7 @@ _lock = threading.Lock()
 _lib = None
 
 GMIN = -5.0        # lower bound of the log-decay (Chapter 5, K3's bounded gate)
+RMS_EPS = 1e-6     # reading: the pages give no epsilon for the head RMSNorm
 CONV_WIDTH = 4     # ShortConv kernel size (infra diagram, KDA card)
 L2_EPS = 1e-6      # reading: the pages give no epsilon for the L2 norm
 
@@ -69,9 +70,11 @@ def _load():
             lib.kda_oracle_l2norm.argtypes = [P, i64, i32, f64]
             lib.kda_oracle_decay_gate.argtypes = [P, i64, f64, P]
             lib.kda_oracle_sigmoid.argtypes = [P, i64, P]
+            lib.kda_oracle_output_gate.argtypes = [P, P, P, i64, i32, f64, P]
             for fn in (lib.kda_oracle_recurrence, lib.kda_oracle_short_conv,
                        lib.kda_oracle_swish, lib.kda_oracle_l2norm,
-                       lib.kda_oracle_decay_gate, lib.kda_oracle_sigmoid):
+                       lib.kda_oracle_decay_gate, lib.kda_oracle_sigmoid,
+                       lib.kda_oracle_output_gate):
                 fn.restype = ctypes.c_int
             _lib = lib
     return _lib
@@ -194,3 +197,14 @@ def prologue(q_raw, k_raw, v_raw, conv_w, z_g=None, z_beta=None,
     g = None if z_g is None else decay_gate(z_g, gmin)
     beta = None if z_beta is None else sigmoid(z_beta)
     return outs[0], outs[1], outs[2], g, beta
+
+
+def output_gate(o, z, w=None, eps: float = RMS_EPS):
+    """Head RMSNorm times sigmoid(gate): o, z [..., d]; w [d] or None."""
+    o, z = _f64(o), _f64(z)
+    d = o.shape[-1]
+    ww = None if w is None else _f64(w)
+    y = np.zeros_like(o)
+    _check(_load().kda_oracle_output_gate(_ptr(o), _ptr(z), _ptr(ww), o.size // d, d, eps,
+                                          _ptr(y)), "output_gate")
+    return y

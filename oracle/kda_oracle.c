@@ -19,8 +19,12 @@
  *        of the state per key channel) and "Inside a KDA Layer".
  *  [D1]  "An infra-oriented diagram of Kimi K3" -- "Kimi Delta Attention:
  *        fixed-state sequence mixing" (width-4 depthwise causal conv, Swish,
- *        L2Norm of q and k, scaled sigmoid, beta = sigmoid) and the packed-token
- *        note (cumulative sequence offsets keep document boundaries).
+ *        L2Norm of q and k, scaled sigmoid, beta = sigmoid; "Head RMSNorm +
+ *        gate, full-rank 7168 -> 12288 gate") and the packed-token note
+ *        (cumulative sequence offsets keep document boundaries).
+ *  [B5g] "From GPT-2 to Kimi K3", Chapter 5, "A third gate: control what
+ *        leaves the module" (head-wise RMSNorm and sigmoid(W_g x) after the
+ *        recurrent read).
  *
  * Readings taken where the pages are silent (each listed in the design notes):
  *  - query scale 1: o_t = S_t^T q_t exactly as written;
@@ -29,7 +33,10 @@
  *    current token (y_t = sum_j w_j x_{t-3+j});
  *  - L2 norm: x / sqrt(sum x^2 + eps), eps passed by the caller;
  *  - documents in a packed batch never see each other (state and conv
- *    history restart at every cu_seqlens entry).
+ *    history restart at every cu_seqlens entry);
+ *  - output gate: RMSNorm over the d channels of one head and token,
+ *    x / sqrt(mean x^2 + eps) * w with a per-channel weight w shared by the
+ *    heads, then times sigmoid of the gate logit of the same channel.
  *
  * Every routine is written as the plain definition, element by element, in
  * double precision.  OpenMP only distributes independent (document, head)
@@ -259,5 +266,30 @@ int kda_oracle_sigmoid(const double *z, int64_t count, double *out)
         return KDA_ORACLE_BAD_ARGS;
     for (int64_t i = 0; i < count; ++i)
         out[i] = 1.0 / (1.0 + exp(-z[i]));
+    return KDA_ORACLE_OK;
+}
+
+/*
+ * Head-wise RMSNorm and the full-rank output gate [B5g], [D1], [E3] ("The
+ * result is normalised, multiplied element-wise by an output gate"):
+ *   y[r, c] = o[r, c] / sqrt(mean_c' o[r, c']^2 + eps) * w[c] * sigmoid(z[r, c])
+ * o, z, y : [rows, d] (one row per token and head);  w : [d] or NULL (ones).
+ */
+int kda_oracle_output_gate(const double *o, const double *z, const double *w,
+                           int64_t rows, int32_t d, double eps, double *y)
+{
+    if (o == NULL || z == NULL || y == NULL || rows < 0 || d < 1 || eps < 0.0)
+        return KDA_ORACLE_BAD_ARGS;
+    for (int64_t r = 0; r < rows; ++r) {
+        const double *orow = o + (size_t)r * d;
+        double ss = 0.0;
+        for (int32_t c = 0; c < d; ++c)
+            ss += orow[c] * orow[c];
+        const double inv_rms = 1.0 / sqrt(ss / d + eps);
+        for (int32_t c = 0; c < d; ++c) {
+            const double gate = 1.0 / (1.0 + exp(-z[(size_t)r * d + c]));
+            y[(size_t)r * d + c] = orow[c] * inv_rms * (w ? w[c] : 1.0) * gate;
+        }
+    }
     return KDA_ORACLE_OK;
 }

@@ -458,3 +458,34 @@ def test_planted_mistakes_are_caught(mistake):
     ok_out, ok_fin = _planted(q, k, v, g, beta, S0, "none")
     close(ok_out, ref_out, rtol=1e-12, atol=1e-12)
     assert not (np.allclose(bad_out, ref_out, rtol=1e-6) and np.allclose(bad_fin, ref_fin, rtol=1e-6))
+
+
+# ---------------------------------------------------------------- output gate
+
+def test_output_gate_matches_torch_rms_norm_and_sigmoid():
+    """Head RMSNorm x sigmoid(gate) (From GPT-2 to Kimi K3, Chapter 5 'A third
+    gate'; infra diagram 'Head RMSNorm + gate') equals torch's rms_norm and
+    sigmoid in fp64."""
+    rng = np.random.default_rng(17)
+    o = rng.standard_normal((30, 4, 16)) * 3
+    z = rng.standard_normal((30, 4, 16)) * 2
+    w = rng.uniform(0.5, 1.5, 16)
+    y = oracle.output_gate(o, z, w, eps=1e-6)
+    ref = torch.nn.functional.rms_norm(torch.tensor(o), (16,), torch.tensor(w), eps=1e-6) \
+        * torch.sigmoid(torch.tensor(z))
+    close(y, ref.numpy(), rtol=1e-12, atol=1e-14)
+
+
+def test_output_gate_invariants():
+    """Scale invariance of the norm, odd symmetry, unit RMS when the gate is
+    open and w = 1, and sigmoid(0) = 1/2."""
+    rng = np.random.default_rng(18)
+    o = rng.standard_normal((20, 8))
+    z = rng.standard_normal((20, 8))
+    y = oracle.output_gate(o, z, eps=0.0)
+    close(oracle.output_gate(7.5 * o, z, eps=0.0), y, rtol=1e-13, atol=1e-15)
+    close(oracle.output_gate(-o, z, eps=0.0), -y, rtol=0, atol=0)
+    open_ = oracle.output_gate(o, np.full_like(z, 60.0), eps=0.0)
+    close(np.sqrt(np.mean(open_ ** 2, axis=-1)), np.ones(20), rtol=1e-13, atol=0)
+    half = oracle.output_gate(o, np.zeros_like(z), eps=0.0)
+    close(2 * half, open_, rtol=1e-14, atol=1e-16)
