@@ -434,7 +434,7 @@ def run_reference(args, dist):
             vals.append(cb["value"])
     value = statistics.mean(vals)
     line = base_line(args, dist, "f64")
-    line.update({"impl": "reference", "value": round(value, 2), "n_gpus": 1,
+    line.update({"impl": "reference", "value": round(value, 2), "n_gpus": dist.world,
                  "ms_per_step": round(4096 / value * 1e3, 2),
                  "cpu_baseline": dict(cb, value=round(value, 2)),
                  "e2e": {"value": round(value, 2), "unit": "tokens/s",

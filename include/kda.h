@@ -204,6 +204,18 @@ KDA_API kda_status kda_output_gate(const void *o, const void *z, const float *we
                                    kda_dims dims, float eps, void *y, void *stream);
 
 /*
+ * Diagnostic of the bounded device-side waits (the paper has no counterpart).
+ * Every wait of the tensor-core prefill gives up after a time limit,
+ * records KDA_DEVICE_TIMEOUT in the workspace status word and lets its CTA
+ * leave, instead of hanging.  This call launches one CTA that waits on a
+ * shared-memory barrier nothing arrives on, with the same wait and a limit
+ * of limit_ns (0 .. 1e9); afterwards kda_get_device_status reports
+ * KDA_ERR_TIMEOUT.  Clears the status word first; never faults.
+ */
+KDA_API kda_status kda_selftest_wait(int64_t limit_ns, void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/*
  * Waits for `stream`, then copies the workspace status word (one of the
  * KDA_DEVICE_* values) to *status_out.  Returns KDA_ERR_DEVICE /
  * KDA_ERR_TIMEOUT when the word is set, KDA_OK when it is clear.

@@ -262,6 +262,21 @@ kda_status kda_output_gate(const void *o, const void *z, const float *weight, in
     return KDA_OK;
 }
 
+kda_status kda_selftest_wait(int64_t limit_ns, void *workspace, size_t workspace_bytes,
+                             void *stream) {
+    g_last_error[0] = '\0';
+    if (limit_ns < 0 || limit_ns > 1000000000)
+        return fail(KDA_ERR_INVALID, "limit_ns must be in [0, 1e9]%s");
+    KDA_TRY(need(workspace, "workspace"));
+    if (workspace_bytes < kStatusBytes) return fail(KDA_ERR_INVALID, "workspace too small%s");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    int32_t *status = static_cast<int32_t *>(workspace);
+    cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
+    if (err == cudaSuccess) err = kda::launch_selftest_wait((uint64_t)limit_ns, status, s);
+    if (err != cudaSuccess) return cuda_fail(err, "self-test launch");
+    return KDA_OK;
+}
+
 kda_status kda_get_device_status(const void *workspace, int32_t *status_out,
                                  void *stream) {
     g_last_error[0] = '\0';

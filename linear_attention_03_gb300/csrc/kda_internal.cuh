@@ -122,6 +122,8 @@ cudaError_t launch_verify(const void *q, const void *k, const void *v, const flo
 cudaError_t launch_output_gate(const void *o, const void *z, const float *weight, int64_t rows,
                                int32_t D, kda_dtype dt, float eps, void *y, cudaStream_t stream);
 
+cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t *status, cudaStream_t stream);
+
 // Tensor-core chunked prefill (d = 128, bf16 q/k/v).
 bool chunk_prefill_supported(int32_t D, kda_dtype dt);
 cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, const float *g,

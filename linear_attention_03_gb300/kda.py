@@ -28,7 +28,7 @@ KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT = 0, 1, 2
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
            "kda_prologue", "kda_get_device_status", "kda_last_error",
            "kda_kernel_launches", "kda_decode_step_conv", "kda_decode_verify",
-           "kda_output_gate", "kda_prefill_noalloc")
+           "kda_output_gate", "kda_prefill_noalloc", "kda_selftest_wait")
 
 
 class kda_dims(ctypes.Structure):
@@ -48,6 +48,8 @@ lib.kda_get_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
 lib.kda_decode_step_conv.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
 lib.kda_decode_verify.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i32, kda_dims, _P, _P, _P]
 lib.kda_output_gate.argtypes = [_P, _P, _P, _i64, kda_dims, ctypes.c_float, _P, _P]
+lib.kda_selftest_wait.argtypes = [_i64, _P, _sz, _P]
+lib.kda_selftest_wait.restype = ctypes.c_int
 lib.kda_last_error.argtypes = []
 lib.kda_last_error.restype = ctypes.c_char_p
 lib.kda_kernel_launches.argtypes = []

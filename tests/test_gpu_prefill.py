@@ -3,6 +3,8 @@ shapes that span several 64-token chunks with a ragged tail, packed
 documents (including empty and one-token ones), every supported head size
 and dtype, and the structural invariants (split runs, aliasing, bad
 offsets).  Tolerances: tests/kda_testlib.py."""
+import ctypes
+
 import numpy as np
 import pytest
 import torch
@@ -94,4 +96,17 @@ def test_bad_offsets_set_the_device_status(kda):
     good = torch.tensor([0, 20, 40], dtype=torch.int32, device="cuda")
     kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, good,
                     workspace=ws)
+    assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_OK
+
+
+def test_bounded_wait_reports_timeout(kda):
+    """A device-side wait on a barrier nothing arrives on gives up after its
+    limit and records KDA_DEVICE_TIMEOUT; the context stays usable."""
+    ws = torch.zeros(256, dtype=torch.uint8, device="cuda")
+    st = kda.lib.kda_selftest_wait(2_000_000, ctypes.c_void_p(ws.data_ptr()), ws.numel(),
+                                   ctypes.c_void_p(torch.cuda.current_stream().cuda_stream))
+    assert st == kda.KDA_OK
+    assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_TIMEOUT
+    inp = to_device(synth.custom(20, 2, 128, torch.bfloat16, seed=505))
+    kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, workspace=ws)
     assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_OK
