@@ -43,8 +43,6 @@
 // leaves after draining its own outstanding copies.
 #include <cuda.h>
 
-#include <type_traits>
-
 #include "kda_internal.cuh"
 #include "kda_tc.cuh"
 
@@ -72,7 +70,7 @@ constexpr uint32_t OFF_BUF1 = 49152;
 constexpr uint32_t OFF_G = 65536;
 // Gram region: cumsum scratch, the Gram operands, afterwards P / L / Tb / U
 constexpr uint32_t OFF_GR = 98304;
-constexpr uint32_t GR_CS = 0;          // fp32 [16][128] partial sums of the cumsum
+constexpr uint32_t GR_CS = 16384;      // fp32 [16][128] partial sums of the cumsum (L area)
 constexpr uint32_t GR_GA = 0;          // [kE; qE] K-major, 2 halves x 16384
 constexpr uint32_t GR_RT = 32768;      // R rows 0..159 K-major, 2 halves x 20480
 constexpr uint32_t RT_HALF = 20480;
@@ -81,7 +79,7 @@ constexpr uint32_t GR_L = 16384;       // L, then T: fp32 [64][LST]
 constexpr uint32_t LST = 68;           // padded row stride (floats)
 constexpr uint32_t GR_TB = 34816;      // [Tb; 0] K-major [128][128 B]
 constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]
-constexpr uint32_t GR_Y = 67584;       // fp32 [16][48] scratch of the UT solve
+constexpr uint32_t GR_Y = 67584;       // spare
 // bf16 copy of the state, MN-major B: two N halves of [128 rows][128 B]
 constexpr uint32_t OFF_S = 172032;
 // per-channel vectors of the chunk
@@ -89,8 +87,8 @@ constexpr uint32_t OFF_VEC = 204800;
 constexpr uint32_t VEC_GS = 0;          // bf16 [4][128]  e^{s_a}
 constexpr uint32_t VEC_KH = 1024;       // bf16 [4][128]  e^{G_63 - e_a}
 constexpr uint32_t VEC_PV = 2048;       // bf16 [10][128] e^{s_a - e_b}, b <= a
-constexpr uint32_t VEC_DEC = 4608;      // fp32 [128]     e^{G_63}
-constexpr uint32_t OFF_BETA = OFF_VEC + 5120;       // [64] fp32
+constexpr uint32_t VEC_DEC = 4608;      // fp32 [2][128]  e^{G_63} of this chunk and the next
+constexpr uint32_t OFF_BETA = OFF_VEC + 5632;       // [64] fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;        // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 64;         // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
@@ -233,6 +231,77 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         if (!mbar_wait(sb + OFF_BAR + bar, c & 1)) misc[1] = 1;
     };
 
+    // cumulative log-decay in log2 units, in place in the g tile: thread =
+    // (4 channels, 4 tokens), two-level scan over the 16 token groups
+    auto do_cumsum = [&](int lenx) {
+        const int c4 = tid & 31, tg = tid >> 5;
+        float4 x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 4 * tg + i;
+            x[i] = (t < lenx) ? SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4)
+                              : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int i = 1; i < 4; ++i) {
+            x[i].x += x[i - 1].x; x[i].y += x[i - 1].y;
+            x[i].z += x[i - 1].z; x[i].w += x[i - 1].w;
+        }
+        SM_F4(OFF_GR + GR_CS + (uint32_t)(tg * kD + 4 * c4) * 4) = x[3];
+        __syncthreads();
+        float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int g2 = 0; g2 < tg; ++g2) {
+            const float4 p = SM_F4(OFF_GR + GR_CS + (uint32_t)(g2 * kD + 4 * c4) * 4);
+            off.x += p.x; off.y += p.y; off.z += p.z; off.w += p.w;
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int t = 4 * tg + i;
+            SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4) =
+                make_float4((x[i].x + off.x) * kLog2e, (x[i].y + off.y) * kLog2e,
+                            (x[i].z + off.z) * kLog2e, (x[i].w + off.w) * kLog2e);
+        }
+        __syncthreads();
+    };
+    // per-channel tile vectors of the chunk whose G is in the g tile
+    auto do_vectors = [&](int decslot) {
+        const int ch = tid & 127, part = tid >> 7;
+        auto G = [&](int t) { return t < 0 ? 0.f : SM_F(OFF_G + (uint32_t)(t * kD + ch) * 4); };
+        const float g63 = G(63);
+        if (part == 0) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                SM_H(OFF_VEC + VEC_GS + a * 256 + ch * 2) = __float2bfloat16_rn(ex2(G(16 * a - 1)));
+            SM_F(OFF_VEC + VEC_DEC + decslot * 512 + ch * 4) = ex2(g63);
+        } else if (part == 1) {
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+                SM_H(OFF_VEC + VEC_KH + a * 256 + ch * 2) =
+                    __float2bfloat16_rn(ex2(g63 - G(16 * a + 15)));
+        } else {
+            // pairs (a, b <= a) in order; part 2 takes 0..4, part 3 takes 5..9
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b <= a; ++b) {
+                    const int idx = a * (a + 1) / 2 + b;
+                    if ((idx < 5) == (part == 2))
+                        SM_H(OFF_VEC + VEC_PV + idx * 256 + ch * 2) =
+                            __float2bfloat16_rn(ex2(G(16 * a - 1) - G(16 * b + 15)));
+                }
+        }
+        __syncthreads();
+    };
+    auto chunk_len = [&](int cc) {
+        const int64_t rem = eos - (bos + (int64_t)cc * kC);
+        return rem < kC ? static_cast<int>(rem) : kC;
+    };
+    if (nchunks > 0) {
+        wait_tma(BAR_G, 0);
+        do_cumsum(chunk_len(0));
+        do_vectors(0);
+    }
+
     const uint32_t gr = sb + OFF_GR;    // shared address of the Gram region (descriptors)
     int c = 0;
     for (; c < nchunks; ++c) {
@@ -240,73 +309,13 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         const int lenc = (eos - t0) < kC ? static_cast<int>(eos - t0) : kC;
         const uint32_t kbuf = buf_off(c), vbuf = buf_off(c + 1);
 
-        // ---------------- step 1: inputs, beta, cumulative log-decay (log2 units)
+        // ---------------- step 1: this chunk's q/k tiles and beta (G and the tile
+        // vectors of this chunk were computed during the previous chunk)
         if (tid < kC) SM_F(OFF_BETA + 4 * tid) = beta_next;
         wait_tma(BAR_Q, c);
         wait_tma(BAR_K, c);
-        wait_tma(BAR_G, c);
-        {
-            // thread = (4 channels, 4 tokens); two-level scan over the 16 token groups
-            const int c4 = tid & 31, tg = tid >> 5;
-            float4 x[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 4 * tg + i;
-                x[i] = (t < lenc) ? SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4)
-                                  : make_float4(0.f, 0.f, 0.f, 0.f);
-            }
-#pragma unroll
-            for (int i = 1; i < 4; ++i) {
-                x[i].x += x[i - 1].x; x[i].y += x[i - 1].y;
-                x[i].z += x[i - 1].z; x[i].w += x[i - 1].w;
-            }
-            SM_F4(OFF_GR + GR_CS + (uint32_t)(tg * kD + 4 * c4) * 4) = x[3];
-            __syncthreads();
-            float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int g2 = 0; g2 < tg; ++g2) {
-                const float4 p = SM_F4(OFF_GR + GR_CS + (uint32_t)(g2 * kD + 4 * c4) * 4);
-                off.x += p.x; off.y += p.y; off.z += p.z; off.w += p.w;
-            }
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int t = 4 * tg + i;
-                SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4) =
-                    make_float4((x[i].x + off.x) * kLog2e, (x[i].y + off.y) * kLog2e,
-                                (x[i].z + off.z) * kLog2e, (x[i].w + off.w) * kLog2e);
-            }
-        }
         __syncthreads();
         if (misc[1]) break;
-
-        // ---------------- per-channel tile vectors
-        {
-            const int ch = tid & 127, part = tid >> 7;
-            auto G = [&](int t) { return t < 0 ? 0.f : SM_F(OFF_G + (uint32_t)(t * kD + ch) * 4); };
-            const float g63 = G(63);
-            if (part == 0) {
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-                    SM_H(OFF_VEC + VEC_GS + a * 256 + ch * 2) = __float2bfloat16_rn(ex2(G(16 * a - 1)));
-                SM_F(OFF_VEC + VEC_DEC + ch * 4) = ex2(g63);
-            } else if (part == 1) {
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-                    SM_H(OFF_VEC + VEC_KH + a * 256 + ch * 2) =
-                        __float2bfloat16_rn(ex2(g63 - G(16 * a + 15)));
-            } else {
-                // pairs (a, b <= a) in order; part 2 takes 0..4, part 3 takes 5..9
-#pragma unroll
-                for (int a = 0; a < 4; ++a)
-#pragma unroll
-                    for (int b = 0; b <= a; ++b) {
-                        const int idx = a * (a + 1) / 2 + b;
-                        if ((idx < 5) == (part == 2))
-                            SM_H(OFF_VEC + VEC_PV + idx * 256 + ch * 2) =
-                                __float2bfloat16_rn(ex2(G(16 * a - 1) - G(16 * b + 15)));
-                    }
-            }
-        }
-        __syncthreads();
 
         // ---------------- step 2: operands.  thread = (row tile a, 2 rows, 8 channels)
         {
@@ -418,10 +427,8 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     }
                 }
             }
-            // rows 0..63 of [0; P] and rows 64..127 of [Tb; 0] are zero
-            const uint4 z = make_uint4(0, 0, 0, 0);
-            SM_U4(OFF_GR + GR_P + sw128_off(tid >> 3, tid & 7)) = z;
-            SM_U4(OFF_GR + GR_TB + sw128_off(64 + (tid >> 3), tid & 7)) = z;
+            // rows 0..63 of [0; P] are zero
+            SM_U4(OFF_GR + GR_P + sw128_off(tid >> 3, tid & 7)) = make_uint4(0, 0, 0, 0);
         }
         tc_fence_before();
         __syncthreads();
@@ -451,73 +458,75 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 for (int i = 0; i < 16; ++i) SM_F(blk + (uint32_t)(i * LST + col) * 4) = x[i];
             }
             __syncthreads();
-            // 5b: block rows a = 1..3.  Y_b = sum_{m=b}^{a-1} L_am T_mb, then
-            // T_ab = -T_aa Y_b.  Group g (64 threads) owns block column b = g;
-            // thread = (row r, 4-column quad q); loop bounds are compile-time.
+            // 5b: off-diagonal blocks.  With D = blockdiag(T_aa) and N the
+            // strictly block-lower part of L, (I + L) = (I + N D) D^-1, so
+            // T = D (I + M)^-1 = D (I - M + M^2 - M^3) with M = N D (block
+            // nilpotent).  Four stages of independent 16x16x16 products; a
+            // group of 64 threads computes one block, thread = (row r, 4-column
+            // quad q4).  Scratch blocks (dense 16x16 fp32) sit in the Tb area.
             const int grp = tid >> 6, r = (tid & 63) >> 2, q4 = tid & 3;
-            const uint32_t Yo = OFF_GR + GR_Y;
-            auto y_stage = [&](auto A_, auto B_) {
-                constexpr int A = decltype(A_)::value, B = decltype(B_)::value;
-                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-#pragma unroll
-                for (int m = B; m < A; ++m)
-#pragma unroll
-                    for (int l4 = 0; l4 < 4; ++l4) {
-                        const float4 lv = SM_F4(Lo + (uint32_t)((16 * A + r) * LST + 16 * m + 4 * l4) * 4);
-                        const float la[4] = {lv.x, lv.y, lv.z, lv.w};
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float4 tv = SM_F4(Lo + (uint32_t)((16 * m + 4 * l4 + e) * LST + 16 * B + 4 * q4) * 4);
-                            float4 &y = (e & 1) ? y1 : y0;
-                            y.x += la[e] * tv.x; y.y += la[e] * tv.y;
-                            y.z += la[e] * tv.z; y.w += la[e] * tv.w;
-                        }
-                    }
-                SM_F4(Yo + (uint32_t)(r * 48 + 16 * B + 4 * q4) * 4) =
-                    make_float4(y0.x + y1.x, y0.y + y1.y, y0.z + y1.z, y0.w + y1.w);
-            };
-            auto t_stage = [&](auto A_, auto B_) {
-                constexpr int A = decltype(A_)::value, B = decltype(B_)::value;
+            const uint32_t Xo = OFF_GR + GR_TB;                 // scratch base
+            auto LB = [&](int a, int b) { return Lo + (uint32_t)(16 * a * LST + 16 * b) * 4; };
+            auto XB = [&](int i) { return Xo + (uint32_t)i * 1024; };
+            // row r, columns 4q4.. of (A B) for 16x16 blocks with row strides sa, sb
+            auto prod = [&](uint32_t A, uint32_t sa, uint32_t B, uint32_t sbs) {
                 float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
 #pragma unroll
                 for (int l4 = 0; l4 < 4; ++l4) {
-                    const float4 tv = SM_F4(Lo + (uint32_t)((16 * A + r) * LST + 16 * A + 4 * l4) * 4);
-                    const float ta[4] = {tv.x, tv.y, tv.z, tv.w};
+                    const float4 av = SM_F4(A + (uint32_t)(r * sa + 4 * l4) * 4);
+                    const float ar[4] = {av.x, av.y, av.z, av.w};
 #pragma unroll
                     for (int e = 0; e < 4; ++e) {
-                        const float4 yv = SM_F4(Yo + (uint32_t)((4 * l4 + e) * 48 + 16 * B + 4 * q4) * 4);
+                        const float4 bv = SM_F4(B + (uint32_t)((4 * l4 + e) * sbs + 4 * q4) * 4);
                         float4 &y = (e & 1) ? y1 : y0;
-                        y.x += ta[e] * yv.x; y.y += ta[e] * yv.y;
-                        y.z += ta[e] * yv.z; y.w += ta[e] * yv.w;
+                        y.x += ar[e] * bv.x; y.y += ar[e] * bv.y;
+                        y.z += ar[e] * bv.z; y.w += ar[e] * bv.w;
                     }
                 }
-                SM_F4(Lo + (uint32_t)((16 * A + r) * LST + 16 * B + 4 * q4) * 4) =
-                    make_float4(-(y0.x + y1.x), -(y0.y + y1.y), -(y0.z + y1.z), -(y0.w + y1.w));
+                return make_float4(y0.x + y1.x, y0.y + y1.y, y0.z + y1.z, y0.w + y1.w);
             };
-            using I0 = std::integral_constant<int, 0>;
-            using I1 = std::integral_constant<int, 1>;
-            using I2 = std::integral_constant<int, 2>;
-            using I3 = std::integral_constant<int, 3>;
-            // block row 1
-            if (grp == 0) y_stage(I1{}, I0{});
+            auto at = [&](uint32_t A, uint32_t sa) -> float4 & {
+                return SM_F4(A + (uint32_t)(r * sa + 4 * q4) * 4);
+            };
+            auto sub4 = [](float4 a, float4 b) {
+                return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
+            };
+            // scratch: M10 M21 M32 M20 M31 M30 | V20 V31 P30 V30
+            enum { M10 = 0, M21, M32, M20, M31, M30, V20, V31, P30, V30 };
+            // stage 1: M_ab = L_ab T_bb
+            if (grp < 6) {
+                // (a, b) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+                const int a = grp < 3 ? grp + 1 : (grp == 3 ? 2 : 3);
+                const int b = grp < 3 ? grp : (grp == 4 ? 1 : 0);
+                at(XB(grp), 16) = prod(LB(a, b), LST, LB(b, b), LST);
+            }
             __syncthreads();
-            if (grp == 0) t_stage(I1{}, I0{});
+            // stage 2: T_{a,a-1} = -T_aa M_{a,a-1};  V20 = -M20 + M21 M10;
+            //          V31 = -M31 + M32 M21;  P30 = M31 M10
+            if (grp < 3) {
+                const int a = grp + 1;
+                const float4 y = prod(LB(a, a), LST, XB(M10 + grp), 16);
+                at(LB(a, a - 1), LST) = make_float4(-y.x, -y.y, -y.z, -y.w);
+            } else if (grp == 3) {
+                at(XB(V20), 16) = sub4(prod(XB(M21), 16, XB(M10), 16), at(XB(M20), 16));
+            } else if (grp == 4) {
+                at(XB(V31), 16) = sub4(prod(XB(M32), 16, XB(M21), 16), at(XB(M31), 16));
+            } else if (grp == 5) {
+                at(XB(P30), 16) = prod(XB(M31), 16, XB(M10), 16);
+            }
             __syncthreads();
-            // block row 2
-            if (grp == 0) y_stage(I2{}, I0{});
-            else if (grp == 1) y_stage(I2{}, I1{});
+            // stage 3: T20 = T22 V20;  T31 = T33 V31;  V30 = -M30 + P30 - M32 V20
+            if (grp == 0) {
+                at(LB(2, 0), LST) = prod(LB(2, 2), LST, XB(V20), 16);
+            } else if (grp == 1) {
+                at(LB(3, 1), LST) = prod(LB(3, 3), LST, XB(V31), 16);
+            } else if (grp == 2) {
+                at(XB(V30), 16) = sub4(sub4(at(XB(P30), 16), at(XB(M30), 16)),
+                                       prod(XB(M32), 16, XB(V20), 16));
+            }
             __syncthreads();
-            if (grp == 0) t_stage(I2{}, I0{});
-            else if (grp == 1) t_stage(I2{}, I1{});
-            __syncthreads();
-            // block row 3
-            if (grp == 0) y_stage(I3{}, I0{});
-            else if (grp == 1) y_stage(I3{}, I1{});
-            else if (grp == 2) y_stage(I3{}, I2{});
-            __syncthreads();
-            if (grp == 0) t_stage(I3{}, I0{});
-            else if (grp == 1) t_stage(I3{}, I1{});
-            else if (grp == 2) t_stage(I3{}, I2{});
+            // stage 4: T30 = T33 V30
+            if (grp == 0) at(LB(3, 0), LST) = prod(LB(3, 3), LST, XB(V30), 16);
             __syncthreads();
             // 5c: [Tb; 0] rows 0..63, thread = (row t, 8-column chunk)
             {
@@ -528,6 +537,8 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 #pragma unroll
                 for (int e = 0; e < 8; ++e) x[e] = (8 * cb + e <= t) ? tr[e] * bb[e] : 0.f;
                 SM_U4(OFF_GR + GR_TB + sw128_off(t, cb)) = pack_bf16x8(x);
+                // rows 64..127 are zero (the UT scratch used this area)
+                SM_U4(OFF_GR + GR_TB + sw128_off(64 + t, cb)) = make_uint4(0, 0, 0, 0);
             }
         }
         fence_proxy_async();
@@ -546,6 +557,12 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 mma_bf16(tmem + TM_D1, ad, sw128_desc(sb + vbuf + kk * 2048, 8192, 1024), id, kk > 0);
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
+        }
+        // while the tensor core works: G of the next chunk (its g tile was
+        // loaded during step 3; the cumsum scratch is the dead L area)
+        if (c + 1 < nchunks) {
+            wait_tma(BAR_G, c + 1);
+            do_cumsum(chunk_len(c + 1));
         }
         wait_mma();
         // v is consumed: the next chunk's k goes into its buffer
@@ -582,6 +599,8 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
+        // while the tensor core works: the tile vectors of the next chunk
+        if (c + 1 < nchunks) do_vectors((c + 1) & 1);
         wait_mma();
         // q of this chunk is consumed: prefetch the next chunk's
         if (tid == 0 && c + 1 < nchunks) {
@@ -645,13 +664,14 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     }
                 }
             }
-            const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * srow);
+            const float dec = SM_F(OFF_VEC + VEC_DEC + (c & 1) * 512 + 4 * srow);
             float ds[64];    // [D3 | S]
+            tmem_wait_st();  // the previous chunk's store of S has landed
             tmem_ld32x2(tlane + TM_D3 + 32 * qq, tlane + TM_S + 32 * qq, ds);
             float S[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) S[j] = dec * ds[32 + j] + ds[j];
-            tmem_st32(tlane + TM_S + 32 * qq, S);
+            tmem_st32_nowait(tlane + TM_S + 32 * qq, S);
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
                 float x[8];
@@ -678,6 +698,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         }
     } else if (final_state != nullptr) {
         tc_fence_after();
+        tmem_wait_st();
         float S[32];
         tmem_ld32(tlane + TM_S + 32 * qq, S);
         float *dst = final_state + unit * kD * kD + (size_t)srow * kD + 32 * qq;
@@ -685,6 +706,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
+    tmem_wait_st();
     tc_fence_before();
     __syncthreads();
     if (warp == 0) {
