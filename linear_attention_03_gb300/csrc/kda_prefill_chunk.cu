@@ -78,8 +78,8 @@ constexpr uint32_t GR_P = 0;           // [0; P] K-major [128][128 B]
 constexpr uint32_t GR_L = 16384;       // L, then T: fp32 [64][LST]
 constexpr uint32_t LST = 68;           // padded row stride (floats)
 constexpr uint32_t GR_TB = 34816;      // [Tb; 0] K-major [128][128 B]
-constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]
-constexpr uint32_t GR_Y = 67584;       // spare
+constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]; first the
+                                       // block-inverse scratch (10 fp32 16x16 blocks)
 // bf16 copy of the state, MN-major B: two N halves of [128 rows][128 B]
 constexpr uint32_t OFF_S = 172032;
 // per-channel vectors of the chunk
@@ -118,14 +118,77 @@ __device__ __forceinline__ void load8f(const uint8_t *p, float (&x)[8]) {
     x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
 }
 
+// ---- 16x16x16 fp32 products for the block inverse, one warp each, on the
+// warp-synchronous tensor-core path (mma.sync m16n8k8, tf32 in, fp32 out).
+// Every operand is split into two tf32 terms (x = hi + lo) and the three
+// significant cross products are accumulated, which keeps fp32-level accuracy.
+// Fragment layout (g = lane / 4, t = lane % 4): A rows g and g+8, columns t
+// and t+4 of each 8-wide K slice; B K-rows t and t+4, column g; D rows g and
+// g+8, columns 2t and 2t+1 of each 8-wide N tile.
+__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
+    const float r = x - __uint_as_float(hi);
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+}
+__device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
+}
+// acc += sign * A B, A and B row-major 16x16 fp32 in shared memory (row strides sa, sb)
+template <bool NEG>
+__device__ __forceinline__ void gemm16(float (&acc)[2][4], const float *A, int sa, const float *B, int sb,
+                                       int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int ks = 0; ks < 2; ++ks) {
+        const float av[4] = {A[g * sa + 8 * ks + t], A[(g + 8) * sa + 8 * ks + t],
+                             A[g * sa + 8 * ks + t + 4], A[(g + 8) * sa + 8 * ks + t + 4]};
+        uint32_t ah[4], al[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) tf32_split(NEG ? -av[i] : av[i], ah[i], al[i]);
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const float bv[2] = {B[(8 * ks + t) * sb + 8 * nt + g], B[(8 * ks + t + 4) * sb + 8 * nt + g]};
+            uint32_t bh[2], bl[2];
+            tf32_split(bv[0], bh[0], bl[0]);
+            tf32_split(bv[1], bh[1], bl[1]);
+            mma_tf32(acc[nt], al, bh);
+            mma_tf32(acc[nt], ah, bl);
+            mma_tf32(acc[nt], ah, bh);
+        }
+    }
+}
+// D-layout fragments from / to a row-major 16x16 fp32 block (row stride sc)
+__device__ __forceinline__ void load_c16(float (&acc)[2][4], const float *C, int sc, int lane, float scale) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        const float2 lo = *reinterpret_cast<const float2 *>(C + g * sc + 8 * nt + 2 * t);
+        const float2 hi = *reinterpret_cast<const float2 *>(C + (g + 8) * sc + 8 * nt + 2 * t);
+        acc[nt][0] = scale * lo.x; acc[nt][1] = scale * lo.y;
+        acc[nt][2] = scale * hi.x; acc[nt][3] = scale * hi.y;
+    }
+}
+__device__ __forceinline__ void store_c16(const float (&acc)[2][4], float *C, int sc, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+        *reinterpret_cast<float2 *>(C + g * sc + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
+        *reinterpret_cast<float2 *>(C + (g + 8) * sc + 8 * nt + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
+    }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
              const float *init_state, const int32_t *__restrict__ cu, int32_t N, int64_t T,
              int32_t H, __nv_bfloat16 *__restrict__ out, float *final_state,
              int32_t *__restrict__ status) {
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    // 1024-aligned base, derived from the shared array so accesses stay in the shared window
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     const uint32_t sb = smem_u32(smem);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sp = warp & 3;          // TMEM sub-partition (lanes 32*sp .. 32*sp+31)
@@ -433,15 +496,16 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- step 5: T = (I + L)^-1 in fp32, then Tb = T diag(beta)
+        // ---------------- step 5: T = (I + L)^-1 in fp32, written out as [Tb; 0], Tb = T diag(beta)
         {
-            const uint32_t Lo = OFF_GR + GR_L;
+            float *Lf = reinterpret_cast<float *>(smem + OFF_GR + GR_L);
+            const float *betas = reinterpret_cast<const float *>(smem + OFF_BETA);
             // 5a: diagonal 16x16 blocks by forward substitution, column-oriented:
             // once x_i is known every later partial sum takes one FMA, so the
             // dependency chain is one FMA per row.  thread = (block a, column col)
             if (tid < 64) {
                 const int a5 = tid >> 4, col = tid & 15;
-                const uint32_t blk = Lo + (uint32_t)(16 * a5 * LST + 16 * a5) * 4;
+                float *blk = Lf + 16 * a5 * LST + 16 * a5;
                 float x[16], acc[16];
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = 0.f;
@@ -449,96 +513,109 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 for (int i = 0; i < 16; ++i) {
                     x[i] = ((i == col) ? 1.f : 0.f) - acc[i];
 #pragma unroll
-                    for (int k = i + 1; k < 16; ++k)
-                        acc[k] += SM_F(blk + (uint32_t)(k * LST + i) * 4) * x[i];
+                    for (int k = i + 1; k < 16; ++k) acc[k] += blk[k * LST + i] * x[i];
                 }
                 __syncwarp();
-                // every thread of this warp has read its block: write T_aa in place
+                // every thread of this warp has read its block: write T_aa in place,
+                // and its Tb block (zero above the diagonal, as x_i = 0 for i < col)
+                const int j = 16 * a5 + col;
+                const float bj = betas[j];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) SM_F(blk + (uint32_t)(i * LST + col) * 4) = x[i];
+                for (int i = 0; i < 16; ++i) {
+                    blk[i * LST + col] = x[i];
+                    SM_H(OFF_GR + GR_TB + sw128_off(16 * a5 + i, j >> 3) + (j & 7) * 2) =
+                        __float2bfloat16_rn(x[i] * bj);
+                }
             }
             __syncthreads();
             // 5b: off-diagonal blocks.  With D = blockdiag(T_aa) and N the
             // strictly block-lower part of L, (I + L) = (I + N D) D^-1, so
             // T = D (I + M)^-1 = D (I - M + M^2 - M^3) with M = N D (block
-            // nilpotent).  Four stages of independent 16x16x16 products; a
-            // group of 64 threads computes one block, thread = (row r, 4-column
-            // quad q4).  Scratch blocks (dense 16x16 fp32) sit in the Tb area.
-            const int grp = tid >> 6, r = (tid & 63) >> 2, q4 = tid & 3;
-            const uint32_t Xo = OFF_GR + GR_TB;                 // scratch base
-            auto LB = [&](int a, int b) { return Lo + (uint32_t)(16 * a * LST + 16 * b) * 4; };
-            auto XB = [&](int i) { return Xo + (uint32_t)i * 1024; };
-            // row r, columns 4q4.. of (A B) for 16x16 blocks with row strides sa, sb
-            auto prod = [&](uint32_t A, uint32_t sa, uint32_t B, uint32_t sbs) {
-                float4 y0 = make_float4(0.f, 0.f, 0.f, 0.f), y1 = y0;
-#pragma unroll
-                for (int l4 = 0; l4 < 4; ++l4) {
-                    const float4 av = SM_F4(A + (uint32_t)(r * sa + 4 * l4) * 4);
-                    const float ar[4] = {av.x, av.y, av.z, av.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float4 bv = SM_F4(B + (uint32_t)((4 * l4 + e) * sbs + 4 * q4) * 4);
-                        float4 &y = (e & 1) ? y1 : y0;
-                        y.x += ar[e] * bv.x; y.y += ar[e] * bv.y;
-                        y.z += ar[e] * bv.z; y.w += ar[e] * bv.w;
+            // nilpotent).  Stage 1 forms the six M_ab = L_ab T_bb; stage 2 takes
+            //   T_{a,a-1} = -T_aa M_{a,a-1}
+            //   T20 = T22 (M21 M10 - M20),  T31 = T33 (M32 M21 - M31)
+            //   T30 = T33 (M31 M10 - M30 - M32 (M21 M10 - M20))
+            // one warp per output block.  Scratch blocks: fp32, row stride 20.
+            constexpr int XS = 20;
+            float *X = reinterpret_cast<float *>(smem + OFF_GR + GR_U);
+            auto XB = [&](int i) { return X + i * 16 * XS; };
+            auto LB = [&](int a, int b) { return Lf + 16 * a * LST + 16 * b; };
+            enum { M10 = 0, M21, M32, M20, M31, M30, V20A, V31, V20B, V30 };
+            if (warp < 6) {
+                // (a, b) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+                const int a = warp < 3 ? warp + 1 : (warp == 3 ? 2 : 3);
+                const int b = warp < 3 ? warp : (warp == 4 ? 1 : 0);
+                float acc[2][4] = {};
+                gemm16<false>(acc, LB(a, b), LST, LB(b, b), LST, lane);
+                store_c16(acc, XB(warp), XS, lane);
+            } else {
+                // the zero parts of [Tb; 0]: rows 64..127, and the blocks above the
+                // diagonal (row tile a, 16-byte chunks 2(a+1)..7)
+                const uint4 z = make_uint4(0, 0, 0, 0);
+                for (int i = tid - 192; i < 512 + 192; i += kThreads - 192) {
+                    if (i < 512) {
+                        SM_U4(OFF_GR + GR_TB + sw128_off(64 + (i >> 3), i & 7)) = z;
+                    } else {
+                        const int j = i - 512;
+                        const int row = j < 96 ? j / 6 : (j < 160 ? 16 + (j - 96) / 4 : 32 + (j - 160) / 2);
+                        const int ch = j < 96 ? 2 + j % 6 : (j < 160 ? 4 + (j - 96) % 4 : 6 + (j - 160) % 2);
+                        SM_U4(OFF_GR + GR_TB + sw128_off(row, ch)) = z;
                     }
                 }
-                return make_float4(y0.x + y1.x, y0.y + y1.y, y0.z + y1.z, y0.w + y1.w);
-            };
-            auto at = [&](uint32_t A, uint32_t sa) -> float4 & {
-                return SM_F4(A + (uint32_t)(r * sa + 4 * q4) * 4);
-            };
-            auto sub4 = [](float4 a, float4 b) {
-                return make_float4(a.x - b.x, a.y - b.y, a.z - b.z, a.w - b.w);
-            };
-            // scratch: M10 M21 M32 M20 M31 M30 | V20 V31 P30 V30
-            enum { M10 = 0, M21, M32, M20, M31, M30, V20, V31, P30, V30 };
-            // stage 1: M_ab = L_ab T_bb
-            if (grp < 6) {
-                // (a, b) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-                const int a = grp < 3 ? grp + 1 : (grp == 3 ? 2 : 3);
-                const int b = grp < 3 ? grp : (grp == 4 ? 1 : 0);
-                at(XB(grp), 16) = prod(LB(a, b), LST, LB(b, b), LST);
             }
             __syncthreads();
-            // stage 2: T_{a,a-1} = -T_aa M_{a,a-1};  V20 = -M20 + M21 M10;
-            //          V31 = -M31 + M32 M21;  P30 = M31 M10
-            if (grp < 3) {
-                const int a = grp + 1;
-                const float4 y = prod(LB(a, a), LST, XB(M10 + grp), 16);
-                at(LB(a, a - 1), LST) = make_float4(-y.x, -y.y, -y.z, -y.w);
-            } else if (grp == 3) {
-                at(XB(V20), 16) = sub4(prod(XB(M21), 16, XB(M10), 16), at(XB(M20), 16));
-            } else if (grp == 4) {
-                at(XB(V31), 16) = sub4(prod(XB(M32), 16, XB(M21), 16), at(XB(M31), 16));
-            } else if (grp == 5) {
-                at(XB(P30), 16) = prod(XB(M31), 16, XB(M10), 16);
-            }
-            __syncthreads();
-            // stage 3: T20 = T22 V20;  T31 = T33 V31;  V30 = -M30 + P30 - M32 V20
-            if (grp == 0) {
-                at(LB(2, 0), LST) = prod(LB(2, 2), LST, XB(V20), 16);
-            } else if (grp == 1) {
-                at(LB(3, 1), LST) = prod(LB(3, 3), LST, XB(V31), 16);
-            } else if (grp == 2) {
-                at(XB(V30), 16) = sub4(sub4(at(XB(P30), 16), at(XB(M30), 16)),
-                                       prod(XB(M32), 16, XB(V20), 16));
-            }
-            __syncthreads();
-            // stage 4: T30 = T33 V30
-            if (grp == 0) at(LB(3, 0), LST) = prod(LB(3, 3), LST, XB(V30), 16);
-            __syncthreads();
-            // 5c: [Tb; 0] rows 0..63, thread = (row t, 8-column chunk)
-            {
-                const int t = tid >> 3, cb = tid & 7;
-                float x[8], tr[8], bb[8];
-                load8f(smem + Lo + (uint32_t)(t * LST + 8 * cb) * 4, tr);
-                load8f(smem + OFF_BETA + 32 * cb, bb);
+            if (warp < 6) {
+                float acc[2][4] = {};
+                int ta, tb2;               // output block of T
+                float sgn = 1.f;
+                if (warp < 3) {
+                    ta = warp + 1; tb2 = warp; sgn = -1.f;
+                    gemm16<false>(acc, LB(ta, ta), LST, XB(M10 + warp), XS, lane);
+                } else if (warp == 4) {
+                    ta = 3; tb2 = 1;
+                    load_c16(acc, XB(M31), XS, lane, -1.f);
+                    gemm16<false>(acc, XB(M32), XS, XB(M21), XS, lane);
+                    store_c16(acc, XB(V31), XS, lane);
+                    __syncwarp();
+                    float acc2[2][4] = {};
+                    gemm16<false>(acc2, LB(3, 3), LST, XB(V31), XS, lane);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = (8 * cb + e <= t) ? tr[e] * bb[e] : 0.f;
-                SM_U4(OFF_GR + GR_TB + sw128_off(t, cb)) = pack_bf16x8(x);
-                // rows 64..127 are zero (the UT scratch used this area)
-                SM_U4(OFF_GR + GR_TB + sw128_off(64 + t, cb)) = make_uint4(0, 0, 0, 0);
+                    for (int i = 0; i < 8; ++i) acc[i >> 2][i & 3] = acc2[i >> 2][i & 3];
+                } else {
+                    // warps 3 and 5 both form V20 = M21 M10 - M20 (a private copy each)
+                    const int v = warp == 3 ? V20A : V20B;
+                    load_c16(acc, XB(M20), XS, lane, -1.f);
+                    gemm16<false>(acc, XB(M21), XS, XB(M10), XS, lane);
+                    store_c16(acc, XB(v), XS, lane);
+                    __syncwarp();
+                    if (warp == 3) {
+                        ta = 2; tb2 = 0;
+                    } else {
+                        ta = 3; tb2 = 0;
+                        float acc2[2][4];
+                        load_c16(acc2, XB(M30), XS, lane, -1.f);
+                        gemm16<false>(acc2, XB(M31), XS, XB(M10), XS, lane);
+                        gemm16<true>(acc2, XB(M32), XS, XB(v), XS, lane);
+                        store_c16(acc2, XB(V30), XS, lane);
+                        __syncwarp();
+                    }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i >> 2][i & 3] = 0.f;
+                    gemm16<false>(acc, LB(ta, ta), LST, XB(warp == 3 ? v : V30), XS, lane);
+                }
+                // Tb block (ta, tb2) in bf16: rows 16 ta + g (+8), columns 16 tb2 + 8 nt + 2t (+1)
+                const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    const int col = 16 * tb2 + 8 * nt + 2 * t;
+                    const float2 bb = *reinterpret_cast<const float2 *>(betas + col);
+                    float y0[2] = {sgn * acc[nt][0] * bb.x, sgn * acc[nt][1] * bb.y};
+                    float y1[2] = {sgn * acc[nt][2] * bb.x, sgn * acc[nt][3] * bb.y};
+                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_TB + sw128_off(16 * ta + g, 2 * tb2 + nt) + 4 * t) =
+                        pack_bf16x2(y0[0], y0[1]);
+                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_TB + sw128_off(16 * ta + g + 8, 2 * tb2 + nt) + 4 * t) =
+                        pack_bf16x2(y1[0], y1[1]);
+                }
             }
         }
         fence_proxy_async();
