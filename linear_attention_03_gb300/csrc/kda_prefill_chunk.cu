@@ -70,7 +70,6 @@ constexpr uint32_t OFF_BUF1 = 49152;
 constexpr uint32_t OFF_G = 65536;
 // Gram region: cumsum scratch, the Gram operands, afterwards P / L / Tb / U
 constexpr uint32_t OFF_GR = 98304;
-constexpr uint32_t GR_CS = 16384;      // fp32 [16][128] partial sums of the cumsum (L area)
 constexpr uint32_t GR_GA = 0;          // [kE; qE] K-major, 2 halves x 16384
 constexpr uint32_t GR_RT = 32768;      // R rows 0..159 K-major, 2 halves x 20480
 constexpr uint32_t RT_HALF = 20480;
@@ -84,11 +83,9 @@ constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]; f
 constexpr uint32_t OFF_S = 172032;
 // per-channel vectors of the chunk
 constexpr uint32_t OFF_VEC = 204800;
-constexpr uint32_t VEC_GS = 0;          // bf16 [4][128]  e^{s_a}
-constexpr uint32_t VEC_KH = 1024;       // bf16 [4][128]  e^{G_63 - e_a}
-constexpr uint32_t VEC_PV = 2048;       // bf16 [10][128] e^{s_a - e_b}, b <= a
-constexpr uint32_t VEC_DEC = 4608;      // fp32 [2][128]  e^{G_63} of this chunk and the next
-constexpr uint32_t OFF_BETA = OFF_VEC + 5632;       // [64] fp32
+constexpr uint32_t VEC_SEG = 0;         // fp32 [8][128]  sums of g over the 8-token segments
+constexpr uint32_t VEC_DEC = 4096;      // fp32 [128]     e^{G_63} of the chunk
+constexpr uint32_t OFF_BETA = OFF_VEC + 4608;       // [64] fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;        // mbarriers
 constexpr uint32_t OFF_MISC = OFF_BAR + 64;         // tmem base, abort flag
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
@@ -110,13 +107,6 @@ __device__ __forceinline__ uint32_t buf_off(int i) { return (i & 1) ? OFF_BUF1 :
 struct Maps {
     CUtensorMap q, k, v, g;
 };
-
-__device__ __forceinline__ void load8f(const uint8_t *p, float (&x)[8]) {
-    const float4 a = reinterpret_cast<const float4 *>(p)[0];
-    const float4 b = reinterpret_cast<const float4 *>(p)[1];
-    x[0] = a.x; x[1] = a.y; x[2] = a.z; x[3] = a.w;
-    x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
-}
 
 // ---- 16x16x16 fp32 products for the block inverse, one warp each, on the
 // warp-synchronous tensor-core path (mma.sync m16n8k8, tf32 in, fp32 out).
@@ -294,77 +284,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         if (!mbar_wait(sb + OFF_BAR + bar, c & 1)) misc[1] = 1;
     };
 
-    // cumulative log-decay in log2 units, in place in the g tile: thread =
-    // (4 channels, 4 tokens), two-level scan over the 16 token groups
-    auto do_cumsum = [&](int lenx) {
-        const int c4 = tid & 31, tg = tid >> 5;
-        float4 x[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = 4 * tg + i;
-            x[i] = (t < lenx) ? SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4)
-                              : make_float4(0.f, 0.f, 0.f, 0.f);
-        }
-#pragma unroll
-        for (int i = 1; i < 4; ++i) {
-            x[i].x += x[i - 1].x; x[i].y += x[i - 1].y;
-            x[i].z += x[i - 1].z; x[i].w += x[i - 1].w;
-        }
-        SM_F4(OFF_GR + GR_CS + (uint32_t)(tg * kD + 4 * c4) * 4) = x[3];
-        __syncthreads();
-        float4 off = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int g2 = 0; g2 < tg; ++g2) {
-            const float4 p = SM_F4(OFF_GR + GR_CS + (uint32_t)(g2 * kD + 4 * c4) * 4);
-            off.x += p.x; off.y += p.y; off.z += p.z; off.w += p.w;
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int t = 4 * tg + i;
-            SM_F4(OFF_G + (uint32_t)(t * kD + 4 * c4) * 4) =
-                make_float4((x[i].x + off.x) * kLog2e, (x[i].y + off.y) * kLog2e,
-                            (x[i].z + off.z) * kLog2e, (x[i].w + off.w) * kLog2e);
-        }
-        __syncthreads();
-    };
-    // per-channel tile vectors of the chunk whose G is in the g tile
-    auto do_vectors = [&](int decslot) {
-        const int ch = tid & 127, part = tid >> 7;
-        auto G = [&](int t) { return t < 0 ? 0.f : SM_F(OFF_G + (uint32_t)(t * kD + ch) * 4); };
-        const float g63 = G(63);
-        if (part == 0) {
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-                SM_H(OFF_VEC + VEC_GS + a * 256 + ch * 2) = __float2bfloat16_rn(ex2(G(16 * a - 1)));
-            SM_F(OFF_VEC + VEC_DEC + decslot * 512 + ch * 4) = ex2(g63);
-        } else if (part == 1) {
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-                SM_H(OFF_VEC + VEC_KH + a * 256 + ch * 2) =
-                    __float2bfloat16_rn(ex2(g63 - G(16 * a + 15)));
-        } else {
-            // pairs (a, b <= a) in order; part 2 takes 0..4, part 3 takes 5..9
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int b = 0; b <= a; ++b) {
-                    const int idx = a * (a + 1) / 2 + b;
-                    if ((idx < 5) == (part == 2))
-                        SM_H(OFF_VEC + VEC_PV + idx * 256 + ch * 2) =
-                            __float2bfloat16_rn(ex2(G(16 * a - 1) - G(16 * b + 15)));
-                }
-        }
-        __syncthreads();
-    };
-    auto chunk_len = [&](int cc) {
-        const int64_t rem = eos - (bos + (int64_t)cc * kC);
-        return rem < kC ? static_cast<int>(rem) : kC;
-    };
-    if (nchunks > 0) {
-        wait_tma(BAR_G, 0);
-        do_cumsum(chunk_len(0));
-        do_vectors(0);
-    }
-
     const uint32_t gr = sb + OFF_GR;    // shared address of the Gram region (descriptors)
     int c = 0;
     for (; c < nchunks; ++c) {
@@ -372,67 +291,108 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         const int lenc = (eos - t0) < kC ? static_cast<int>(eos - t0) : kC;
         const uint32_t kbuf = buf_off(c), vbuf = buf_off(c + 1);
 
-        // ---------------- step 1: this chunk's q/k tiles and beta (G and the tile
-        // vectors of this chunk were computed during the previous chunk)
+        // ---------------- step 1: this chunk's q/k/g tiles and beta
         if (tid < kC) SM_F(OFF_BETA + 4 * tid) = beta_next;
         wait_tma(BAR_Q, c);
         wait_tma(BAR_K, c);
+        wait_tma(BAR_G, c);
         __syncthreads();
         if (misc[1]) break;
 
-        // ---------------- step 2: operands.  thread = (row tile a, 2 rows, 8 channels)
+        // ---------------- step 2: G and every decay-scaled operand, one pass.
+        // warp = (channel half hh, row tile a, 8-token segment s8 of the tile),
+        // lane = channel pair ch, ch+1: the running sum over the segment is
+        // sequential in registers, the segment offsets go through shared memory,
+        // and each operand row is stored as 32 bf16 pairs (one full 128-byte row).
         {
-            const int a = tid >> 7, r2 = (tid >> 4) & 7, cc = tid & 15;
-            const int half = cc >> 3, c8 = cc & 7, c0 = 8 * cc;
-            float Gs[8], Ge[8];
-            if (a == 0) {
+            const int hh = warp & 1, a = (warp >> 1) & 3, s8 = warp >> 3;
+            const int ch = 64 * hh + 2 * lane;
+            const int seg = 2 * a + s8, tb = 8 * seg;
+            const uint32_t cw = sw128_off(0, lane >> 2) + 4 * (lane & 3);   // row-0 byte offset
+            auto rowoff = [&](int row) { return (uint32_t)(row * 128) + (cw ^ ((row & 7) << 4)); };
+            float2 G[8];
+            {
+                float2 run = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) Gs[e] = 0.f;
-            } else {
-                load8f(smem + OFF_G + (uint32_t)((16 * a - 1) * kD + c0) * 4, Gs);
-            }
-            load8f(smem + OFF_G + (uint32_t)((16 * a + 15) * kD + c0) * 4, Ge);
-            uint4 kE[2], qE[2], kB[2];
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int t = 16 * a + 2 * r2 + i;
-                float Gt[8];
-                load8f(smem + OFF_G + (uint32_t)(t * kD + c0) * 4, Gt);
-                uint4 kv = SM_U4(kbuf + half * 8192 + sw128_off(t, c8));
-                uint4 qv = SM_U4(OFF_A1 + half * 16384 + sw128_off(64 + t, c8));
-                if (t >= lenc) kv = qv = make_uint4(0, 0, 0, 0);
-                float E[8], Eb[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    E[e] = ex2(Gt[e] - Gs[e]);
-                    Eb[e] = ex2(Ge[e] - Gt[e]);
+                for (int i = 0; i < 8; ++i) {
+                    const int t = tb + i;
+                    const float2 gv = (t < lenc) ? *reinterpret_cast<const float2 *>(smem + OFF_G + (uint32_t)(t * kD + ch) * 4)
+                                                 : make_float2(0.f, 0.f);
+                    run.x += gv.x; run.y += gv.y;
+                    G[i] = run;
                 }
-                const uint4 Ep = pack_bf16x8(E), Ebp = pack_bf16x8(Eb);
-                kE[i] = mul_bf16x8(kv, Ep);
-                qE[i] = mul_bf16x8(qv, Ep);
-                kB[i] = mul_bf16x8(kv, Ebp);
+                *reinterpret_cast<float2 *>(smem + OFF_VEC + VEC_SEG + (uint32_t)(seg * kD + ch) * 4) = run;
+            }
+            __syncthreads();
+            // the g tile is consumed: prefetch the next chunk's
+            if (tid == 0 && c + 1 < nchunks) {
+                issue_g(t0 + kC);
+                issued[3] = c + 1;
+            }
+            // segment boundaries (log2 units), as predicated running sums so that no
+            // array is indexed at run time: G before this segment, before tile a
+            // (s_a), after tile a (e_a), before every tile (for the Gram rows), G_63
+            float2 base = make_float2(0.f, 0.f), sa = base, ea = base, g63 = base;
+            float2 tile0[4];
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                if ((m & 1) == 0) tile0[m >> 1] = make_float2(g63.x * kLog2e, g63.y * kLog2e);
+                const float2 sv = *reinterpret_cast<const float2 *>(smem + OFF_VEC + VEC_SEG + (uint32_t)(m * kD + ch) * 4);
+                if (m < seg) { base.x += sv.x; base.y += sv.y; }
+                if (m < 2 * a) { sa.x += sv.x; sa.y += sv.y; }
+                if (m < 2 * a + 2) { ea.x += sv.x; ea.y += sv.y; }
+                g63.x += sv.x; g63.y += sv.y;
+            }
+            base.x *= kLog2e; base.y *= kLog2e;
+            sa.x *= kLog2e; sa.y *= kLog2e;
+            ea.x *= kLog2e; ea.y *= kLog2e;
+            g63.x *= kLog2e; g63.y *= kLog2e;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                G[i].x = base.x + G[i].x * kLog2e;
+                G[i].y = base.y + G[i].y * kLog2e;
+            }
+            if (warp >= 14)   // e^{G_63}, the state decay of the chunk
+                *reinterpret_cast<float2 *>(smem + OFF_VEC + VEC_DEC + 4 * ch) = make_float2(ex2(g63.x), ex2(g63.y));
+            // e^{s_ap - e_a} for the Gram right operand rows of tiles ap >= a
+            float2 pv[4];
+#pragma unroll
+            for (int ap = 0; ap < 4; ++ap)
+                pv[ap] = make_float2(ex2(tile0[ap].x - ea.x), ex2(tile0[ap].y - ea.y));
+            const float2 gs = make_float2(ex2(sa.x), ex2(sa.y));                    // e^{s_a}
+            const float2 kh = make_float2(ex2(g63.x - ea.x), ex2(g63.y - ea.y));    // e^{G_63 - e_a}
+            float2 kE[8], qE[8], kB[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int t = tb + i;
+                uint32_t kraw = *reinterpret_cast<const uint32_t *>(smem + kbuf + hh * 8192 + rowoff(t));
+                uint32_t qraw = *reinterpret_cast<const uint32_t *>(smem + OFF_A1 + hh * 16384 + rowoff(64 + t));
+                if (t >= lenc) kraw = qraw = 0u;
+                const float2 k2 = unpack_bf16x2(kraw), q2 = unpack_bf16x2(qraw);
+                const float2 E = make_float2(ex2(G[i].x - sa.x), ex2(G[i].y - sa.y));
+                const float2 Eb = make_float2(ex2(ea.x - G[i].x), ex2(ea.y - G[i].y));
+                kE[i] = make_float2(k2.x * E.x, k2.y * E.y);
+                qE[i] = make_float2(q2.x * E.x, q2.y * E.y);
+                kB[i] = make_float2(k2.x * Eb.x, k2.y * Eb.y);
                 // Gram left operand rows t (k) and 64 + t (q)
-                SM_U4(OFF_GR + GR_GA + half * 16384 + sw128_off(t, c8)) = kE[i];
-                SM_U4(OFF_GR + GR_GA + half * 16384 + sw128_off(64 + t, c8)) = qE[i];
+                *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_GA + hh * 16384 + rowoff(t)) =
+                    pack_bf16x2(kE[i].x, kE[i].y);
+                *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_GA + hh * 16384 + rowoff(64 + t)) =
+                    pack_bf16x2(qE[i].x, qE[i].y);
                 // Gram right operand: row gram_off(ap) + t for every row tile ap >= a
 #pragma unroll
                 for (int ap = 0; ap < 4; ++ap) {
                     if (ap < a) continue;
-                    const uint4 pv = SM_U4(OFF_VEC + VEC_PV + (ap * (ap + 1) / 2 + a) * 256 + c0 * 2);
-                    SM_U4(OFF_GR + GR_RT + half * RT_HALF + sw128_off(gram_off(ap) + t, c8)) =
-                        mul_bf16x8(kB[i], pv);
+                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_RT + hh * RT_HALF + rowoff(gram_off(ap) + t)) =
+                        pack_bf16x2(kB[i].x * pv[ap].x, kB[i].y * pv[ap].y);
                 }
             }
             fence_proxy_async();
             __syncthreads();
             // ---------------- step 3: Gram MMAs (8 instructions, N = 160), issued
-            // while the remaining operands are written; the g buffer is free
+            // while the remaining operands are written
             if (tid == 0) {
                 tc_fence_after();
-                if (c + 1 < nchunks) {
-                    issue_g(t0 + kC);
-                    issued[3] = c + 1;
-                }
                 const uint32_t id = idesc_bf16(128, 160, 0, 0);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk) {
@@ -442,15 +402,16 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 }
                 mma_commit(sb + OFF_BAR + BAR_MMA);
             }
-            // Q+ in place, K+ into rows 0..63 of A1, Khat in place of k
-            const uint4 gs = SM_U4(OFF_VEC + VEC_GS + a * 256 + c0 * 2);
-            const uint4 kh = SM_U4(OFF_VEC + VEC_KH + a * 256 + c0 * 2);
+            // Q+ = q e^{G} in place, K+ = k e^{G} into rows 0..63 of A1, Khat = k e^{G_63 - G} in place of k
 #pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                const int t = 16 * a + 2 * r2 + i;
-                SM_U4(OFF_A1 + half * 16384 + sw128_off(64 + t, c8)) = mul_bf16x8(qE[i], gs);
-                SM_U4(OFF_A1 + half * 16384 + sw128_off(t, c8)) = mul_bf16x8(kE[i], gs);
-                SM_U4(kbuf + half * 8192 + sw128_off(t, c8)) = mul_bf16x8(kB[i], kh);
+            for (int i = 0; i < 8; ++i) {
+                const int t = tb + i;
+                *reinterpret_cast<uint32_t *>(smem + OFF_A1 + hh * 16384 + rowoff(64 + t)) =
+                    pack_bf16x2(qE[i].x * gs.x, qE[i].y * gs.y);
+                *reinterpret_cast<uint32_t *>(smem + OFF_A1 + hh * 16384 + rowoff(t)) =
+                    pack_bf16x2(kE[i].x * gs.x, kE[i].y * gs.y);
+                *reinterpret_cast<uint32_t *>(smem + kbuf + hh * 8192 + rowoff(t)) =
+                    pack_bf16x2(kB[i].x * kh.x, kB[i].y * kh.y);
             }
         }
         fence_proxy_async();
@@ -635,12 +596,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
-        // while the tensor core works: G of the next chunk (its g tile was
-        // loaded during step 3; the cumsum scratch is the dead L area)
-        if (c + 1 < nchunks) {
-            wait_tma(BAR_G, c + 1);
-            do_cumsum(chunk_len(c + 1));
-        }
         wait_mma();
         // v is consumed: the next chunk's k goes into its buffer
         if (tid == 0 && c + 1 < nchunks) {
@@ -676,8 +631,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
-        // while the tensor core works: the tile vectors of the next chunk
-        if (c + 1 < nchunks) do_vectors((c + 1) & 1);
         wait_mma();
         // q of this chunk is consumed: prefetch the next chunk's
         if (tid == 0 && c + 1 < nchunks) {
@@ -741,7 +694,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     }
                 }
             }
-            const float dec = SM_F(OFF_VEC + VEC_DEC + (c & 1) * 512 + 4 * srow);
+            const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * srow);
             float ds[64];    // [D3 | S]
             tmem_wait_st();  // the previous chunk's store of S has landed
             tmem_ld32x2(tlane + TM_D3 + 32 * qq, tlane + TM_S + 32 * qq, ds);
