@@ -66,7 +66,9 @@ constexpr uint32_t OFF_A1 = 0;
 // BUF[(c + 1) & 1] (the MN-major B operand of Ut = Tb V as loaded)
 constexpr uint32_t OFF_BUF0 = 32768;
 constexpr uint32_t OFF_BUF1 = 49152;
-// g tile fp32 [64][128] (TMA, no swizzle) -> log2e * G in place
+// g tile fp32 [64][128] (TMA, no swizzle); once scanned, the staging tile of the
+// previous chunk's outputs (bf16, two 64-column halves, 128-byte swizzle) for a
+// bulk tensor store
 constexpr uint32_t OFF_G = 65536;
 // Gram region: cumsum scratch, the Gram operands, afterwards P / L / Tb / U
 constexpr uint32_t OFF_GR = 98304;
@@ -74,8 +76,8 @@ constexpr uint32_t GR_GA = 0;          // [kE; qE] K-major, 2 halves x 16384
 constexpr uint32_t GR_RT = 32768;      // R rows 0..159 K-major, 2 halves x 20480
 constexpr uint32_t RT_HALF = 20480;
 constexpr uint32_t GR_P = 0;           // [0; P] K-major [128][128 B]
-constexpr uint32_t GR_L = 16384;       // L, then T: fp32 [64][LST]
-constexpr uint32_t LST = 68;           // padded row stride (floats)
+constexpr uint32_t GR_L = 16384;       // L, then T: fp32, stored transposed ([column][row], stride LST)
+constexpr uint32_t LST = 72;           // padded stride (floats)
 constexpr uint32_t GR_TB = 34816;      // [Tb; 0] K-major [128][128 B]
 constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]; first the
                                        // block-inverse scratch (10 fp32 16x16 blocks)
@@ -87,7 +89,7 @@ constexpr uint32_t VEC_SEG = 0;         // fp32 [8][128]  sums of g over the 8-t
 constexpr uint32_t VEC_DEC = 4096;      // fp32 [128]     e^{G_63} of the chunk
 constexpr uint32_t OFF_BETA = OFF_VEC + 4608;       // [64] fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;        // mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 64;         // tmem base, abort flag
+constexpr uint32_t OFF_MISC = OFF_BAR + 64;         // tmem base, abort flag, last g chunk loaded
 constexpr uint32_t SMEM_USED = OFF_MISC + 16;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 
@@ -95,9 +97,8 @@ constexpr uint32_t BAR_Q = 0, BAR_K = 8, BAR_V = 16, BAR_G = 24, BAR_MMA = 32;
 
 // TMEM columns
 constexpr uint32_t TM_D1 = 0;     // [U ; O] accumulator
-constexpr uint32_t TM_G = 128;    // Gram blocks (160 columns), then W, then Khat^T U
-constexpr uint32_t TM_D3 = 128;
-constexpr uint32_t TM_S = 288;    // fp32 state, 128 columns
+constexpr uint32_t TM_G = 128;    // Gram blocks (160 columns), then W
+constexpr uint32_t TM_S = 288;    // fp32 state, 128 columns; Khat^T U accumulates into it
 constexpr uint32_t TM_COLS = 512;
 
 // first row / column of row tile a inside the stacked Gram operand / result
@@ -105,7 +106,7 @@ __device__ __forceinline__ uint32_t gram_off(int a) { return 8u * a * (a + 1); }
 __device__ __forceinline__ uint32_t buf_off(int i) { return (i & 1) ? OFF_BUF1 : OFF_BUF0; }
 
 struct Maps {
-    CUtensorMap q, k, v, g;
+    CUtensorMap q, k, v, g, o;
 };
 
 // ---- 16x16x16 fp32 products for the block inverse, one warp each, on the
@@ -127,29 +128,39 @@ __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], 
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]));
 }
-// acc += sign * A B, A and B row-major 16x16 fp32 in shared memory (row strides sa, sb)
-template <bool NEG>
+// acc += sign * A B for 16x16 fp32 blocks in shared memory: A(r, k) at A[r sa + k]
+// (or A[k sa + r] when AT), B(k, n) at B[k sb + n] (or B[n sb + k] when BT)
+template <bool NEG, bool AT, bool BT>
 __device__ __forceinline__ void gemm16(float (&acc)[2][4], const float *A, int sa, const float *B, int sb,
                                        int lane) {
     const int g = lane >> 2, t = lane & 3;
+    auto Ael = [&](int r, int k) { return AT ? A[k * sa + r] : A[r * sa + k]; };
+    auto Bel = [&](int k, int n) { return BT ? B[n * sb + k] : B[k * sb + n]; };
+    // the three cross products go to separate accumulators, so that no MMA waits
+    // on the previous one's result for more than the two K slices
+    float p[3][2][4] = {};
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
-        const float av[4] = {A[g * sa + 8 * ks + t], A[(g + 8) * sa + 8 * ks + t],
-                             A[g * sa + 8 * ks + t + 4], A[(g + 8) * sa + 8 * ks + t + 4]};
+        const float av[4] = {Ael(g, 8 * ks + t), Ael(g + 8, 8 * ks + t), Ael(g, 8 * ks + t + 4),
+                             Ael(g + 8, 8 * ks + t + 4)};
         uint32_t ah[4], al[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) tf32_split(NEG ? -av[i] : av[i], ah[i], al[i]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const float bv[2] = {B[(8 * ks + t) * sb + 8 * nt + g], B[(8 * ks + t + 4) * sb + 8 * nt + g]};
+            const float bv[2] = {Bel(8 * ks + t, 8 * nt + g), Bel(8 * ks + t + 4, 8 * nt + g)};
             uint32_t bh[2], bl[2];
             tf32_split(bv[0], bh[0], bl[0]);
             tf32_split(bv[1], bh[1], bl[1]);
-            mma_tf32(acc[nt], al, bh);
-            mma_tf32(acc[nt], ah, bl);
-            mma_tf32(acc[nt], ah, bh);
+            mma_tf32(p[0][nt], ah, bh);
+            mma_tf32(p[1][nt], ah, bl);
+            mma_tf32(p[2][nt], al, bh);
         }
     }
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[nt][i] += (p[2][nt][i] + p[1][nt][i]) + p[0][nt][i];
 }
 // D-layout fragments from / to a row-major 16x16 fp32 block (row stride sc)
 __device__ __forceinline__ void load_c16(float (&acc)[2][4], const float *C, int sc, int lane, float scale) {
@@ -170,6 +181,12 @@ __device__ __forceinline__ void store_c16(const float (&acc)[2][4], float *C, in
         *reinterpret_cast<float2 *>(C + (g + 8) * sc + 8 * nt + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
     }
 }
+
+// barrier 1: the six warps of the block inverse only
+__device__ __forceinline__ void ut_sync() { asm volatile("bar.sync 1, 192;" ::: "memory"); }
+// barrier 2: the two diagonal-block warps release the ten other warps (64 + 320)
+__device__ __forceinline__ void diag_done_arrive() { asm volatile("bar.arrive 2, 384;" ::: "memory"); }
+__device__ __forceinline__ void diag_done_wait() { asm volatile("bar.sync 2, 384;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
@@ -202,6 +219,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(sb + OFF_BAR + 8 * i, 1);
         misc[1] = 0;
+        misc[2] = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sb + OFF_MISC, TM_COLS);
@@ -324,10 +342,26 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 *reinterpret_cast<float2 *>(smem + OFF_VEC + VEC_SEG + (uint32_t)(seg * kD + ch) * 4) = run;
             }
             __syncthreads();
-            // the g tile is consumed: prefetch the next chunk's
-            if (tid == 0 && c + 1 < nchunks) {
-                issue_g(t0 + kC);
-                issued[3] = c + 1;
+            // the previous chunk's last MMAs (O += P U, S += Khat^T U) have run
+            // while this chunk loaded and scanned: its P, U and Khat are free now
+            if (c > 0) wait_mma();
+            if (tid == 0) {
+                // the chunk after the next one: into L2 now, so that its loads hit L2
+                if (c + 2 < nchunks) {
+                    const int32_t y2 = (int32_t)(t0 + 2 * kC);
+                    tma_prefetch_2d(&maps.q, h * kD, y2);
+                    tma_prefetch_2d(&maps.q, h * kD + 64, y2);
+                    tma_prefetch_2d(&maps.k, h * kD, y2);
+                    tma_prefetch_2d(&maps.k, h * kD + 64, y2);
+                    tma_prefetch_2d(&maps.v, h * kD, y2);
+                    tma_prefetch_2d(&maps.v, h * kD + 64, y2);
+                    tma_prefetch_2d(&maps.g, h * kD, y2);
+                }
+                // this chunk's v goes into the buffer that held the previous Khat
+                if (c > 0) {
+                    issue_v(t0, vbuf);
+                    issued[2] = c;
+                }
             }
             // segment boundaries (log2 units), as predicated running sums so that no
             // array is indexed at run time: G before this segment, before tile a
@@ -427,16 +461,13 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             tmem_ld32(tlane + TM_G + gram_off(a) + 32 * ch2, G);
             if (mine) {
                 if (sp < 2) {
+                    // L stored transposed: L[t][j] at (j LST + t)
                     const float bt = SM_F(OFF_BETA + 4 * t);
+                    float *Lt = reinterpret_cast<float *>(smem + OFF_GR + GR_L) + t;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4) {
+                    for (int j = 0; j < 32; ++j) {
                         const int jj = 32 * ch2 + j;
-                        float4 v;
-                        v.x = (jj + 0 < t) ? bt * G[j + 0] : 0.f;
-                        v.y = (jj + 1 < t) ? bt * G[j + 1] : 0.f;
-                        v.z = (jj + 2 < t) ? bt * G[j + 2] : 0.f;
-                        v.w = (jj + 3 < t) ? bt * G[j + 3] : 0.f;
-                        SM_F4(OFF_GR + GR_L + (uint32_t)(t * LST + jj) * 4) = v;
+                        Lt[jj * LST] = (jj < t) ? bt * G[j] : 0.f;
                     }
                 } else {
 #pragma unroll
@@ -458,7 +489,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         __syncthreads();
 
         // ---------------- step 5: T = (I + L)^-1 in fp32, written out as [Tb; 0], Tb = T diag(beta)
-        {
+        if (warp < 6) {
             float *Lf = reinterpret_cast<float *>(smem + OFF_GR + GR_L);
             const float *betas = reinterpret_cast<const float *>(smem + OFF_BETA);
             // 5a: diagonal 16x16 blocks by forward substitution, column-oriented:
@@ -466,6 +497,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             // dependency chain is one FMA per row.  thread = (block a, column col)
             if (tid < 64) {
                 const int a5 = tid >> 4, col = tid & 15;
+                // the block in transposed storage: blk[i LST + k] = L[16 a5 + k][16 a5 + i]
                 float *blk = Lf + 16 * a5 * LST + 16 * a5;
                 float x[16], acc[16];
 #pragma unroll
@@ -473,109 +505,182 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     x[i] = ((i == col) ? 1.f : 0.f) - acc[i];
+                    // column i of the block is one contiguous row of the transposed storage
+                    float lc[16];
 #pragma unroll
-                    for (int k = i + 1; k < 16; ++k) acc[k] += blk[k * LST + i] * x[i];
+                    for (int q = 0; q < 4; ++q) {
+                        if (4 * q + 3 <= i) continue;
+                        const float4 v = *reinterpret_cast<const float4 *>(blk + i * LST + 4 * q);
+                        lc[4 * q] = v.x; lc[4 * q + 1] = v.y; lc[4 * q + 2] = v.z; lc[4 * q + 3] = v.w;
+                    }
+#pragma unroll
+                    for (int k = i + 1; k < 16; ++k) acc[k] += lc[k] * x[i];
                 }
                 __syncwarp();
-                // every thread of this warp has read its block: write T_aa in place,
-                // and its Tb block (zero above the diagonal, as x_i = 0 for i < col)
+                // every thread of this warp has read its block: T_aa column col goes in
+                // place (transposed storage, as L), and its Tb column (zero above the
+                // diagonal, as x_i = 0 for i < col)
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+                    *reinterpret_cast<float4 *>(blk + col * LST + 4 * q) =
+                        make_float4(x[4 * q], x[4 * q + 1], x[4 * q + 2], x[4 * q + 3]);
                 const int j = 16 * a5 + col;
                 const float bj = betas[j];
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    blk[i * LST + col] = x[i];
+                for (int i = 0; i < 16; ++i)
                     SM_H(OFF_GR + GR_TB + sw128_off(16 * a5 + i, j >> 3) + (j & 7) * 2) =
                         __float2bfloat16_rn(x[i] * bj);
-                }
+                // the forward substitution waits on shared-memory latency step after
+                // step: the other warps start their traffic only once it is done
+                diag_done_arrive();
             }
-            __syncthreads();
+            ut_sync();
             // 5b: off-diagonal blocks.  With D = blockdiag(T_aa) and N the
             // strictly block-lower part of L, (I + L) = (I + N D) D^-1, so
             // T = D (I + M)^-1 = D (I - M + M^2 - M^3) with M = N D (block
-            // nilpotent).  Stage 1 forms the six M_ab = L_ab T_bb; stage 2 takes
-            //   T_{a,a-1} = -T_aa M_{a,a-1}
-            //   T20 = T22 (M21 M10 - M20),  T31 = T33 (M32 M21 - M31)
-            //   T30 = T33 (M31 M10 - M30 - M32 (M21 M10 - M20))
-            // one warp per output block.  Scratch blocks: fp32, row stride 20.
+            // nilpotent).  Stage 1 forms the six M_ab = L_ab T_bb; stage 2 gives
+            //   T_{a,a-1} = -T_aa M_{a,a-1},  V20 = M21 M10 - M20,
+            //   V31 = M32 M21 - M31,  Y30 = M31 M10 - M30;
+            // stage 3: T20 = T22 V20, T31 = T33 V31 and, with T32 = -T33 M32,
+            //   T30 = T33 (Y30 - M32 V20) = T33 Y30 + T32 V20.
+            // One warp per output block; scratch blocks fp32, row stride 20.
             constexpr int XS = 20;
             float *X = reinterpret_cast<float *>(smem + OFF_GR + GR_U);
             auto XB = [&](int i) { return X + i * 16 * XS; };
-            auto LB = [&](int a, int b) { return Lf + 16 * a * LST + 16 * b; };
-            enum { M10 = 0, M21, M32, M20, M31, M30, V20A, V31, V20B, V30 };
-            if (warp < 6) {
-                // (a, b) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
-                const int a = warp < 3 ? warp + 1 : (warp == 3 ? 2 : 3);
-                const int b = warp < 3 ? warp : (warp == 4 ? 1 : 0);
-                float acc[2][4] = {};
-                gemm16<false>(acc, LB(a, b), LST, LB(b, b), LST, lane);
-                store_c16(acc, XB(warp), XS, lane);
-            } else {
-                // the zero parts of [Tb; 0]: rows 64..127, and the blocks above the
-                // diagonal (row tile a, 16-byte chunks 2(a+1)..7)
-                const uint4 z = make_uint4(0, 0, 0, 0);
-                for (int i = tid - 192; i < 512 + 192; i += kThreads - 192) {
-                    if (i < 512) {
-                        SM_U4(OFF_GR + GR_TB + sw128_off(64 + (i >> 3), i & 7)) = z;
-                    } else {
-                        const int j = i - 512;
-                        const int row = j < 96 ? j / 6 : (j < 160 ? 16 + (j - 96) / 4 : 32 + (j - 160) / 2);
-                        const int ch = j < 96 ? 2 + j % 6 : (j < 160 ? 4 + (j - 96) % 4 : 6 + (j - 160) % 2);
-                        SM_U4(OFF_GR + GR_TB + sw128_off(row, ch)) = z;
-                    }
-                }
-            }
-            __syncthreads();
-            if (warp < 6) {
-                float acc[2][4] = {};
-                int ta, tb2;               // output block of T
-                float sgn = 1.f;
-                if (warp < 3) {
-                    ta = warp + 1; tb2 = warp; sgn = -1.f;
-                    gemm16<false>(acc, LB(ta, ta), LST, XB(M10 + warp), XS, lane);
-                } else if (warp == 4) {
-                    ta = 3; tb2 = 1;
-                    load_c16(acc, XB(M31), XS, lane, -1.f);
-                    gemm16<false>(acc, XB(M32), XS, XB(M21), XS, lane);
-                    store_c16(acc, XB(V31), XS, lane);
-                    __syncwarp();
-                    float acc2[2][4] = {};
-                    gemm16<false>(acc2, LB(3, 3), LST, XB(V31), XS, lane);
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i >> 2][i & 3] = acc2[i >> 2][i & 3];
-                } else {
-                    // warps 3 and 5 both form V20 = M21 M10 - M20 (a private copy each)
-                    const int v = warp == 3 ? V20A : V20B;
-                    load_c16(acc, XB(M20), XS, lane, -1.f);
-                    gemm16<false>(acc, XB(M21), XS, XB(M10), XS, lane);
-                    store_c16(acc, XB(v), XS, lane);
-                    __syncwarp();
-                    if (warp == 3) {
-                        ta = 2; tb2 = 0;
-                    } else {
-                        ta = 3; tb2 = 0;
-                        float acc2[2][4];
-                        load_c16(acc2, XB(M30), XS, lane, -1.f);
-                        gemm16<false>(acc2, XB(M31), XS, XB(M10), XS, lane);
-                        gemm16<true>(acc2, XB(M32), XS, XB(v), XS, lane);
-                        store_c16(acc2, XB(V30), XS, lane);
-                        __syncwarp();
-                    }
-#pragma unroll
-                    for (int i = 0; i < 8; ++i) acc[i >> 2][i & 3] = 0.f;
-                    gemm16<false>(acc, LB(ta, ta), LST, XB(warp == 3 ? v : V30), XS, lane);
-                }
-                // Tb block (ta, tb2) in bf16: rows 16 ta + g (+8), columns 16 tb2 + 8 nt + 2t (+1)
+            // block (a, b) of L or T in the transposed storage: element (r, k) at [k LST + r]
+            auto LB = [&](int a, int b) { return Lf + 16 * b * LST + 16 * a; };
+            enum { M10 = 0, M21, M32, M20, M31, M30, V20, V31, Y30, T32F };
+            // Tb block (ta, tb) = sgn * acc, column-scaled by beta, in bf16:
+            // rows 16 ta + g (+8), columns 16 tb + 8 nt + 2t (+1)
+            auto tb_store = [&](int ta, int tb, float sgn, const float (&acc)[2][4]) {
                 const int g = lane >> 2, t = lane & 3;
 #pragma unroll
                 for (int nt = 0; nt < 2; ++nt) {
-                    const int col = 16 * tb2 + 8 * nt + 2 * t;
+                    const int col = 16 * tb + 8 * nt + 2 * t;
                     const float2 bb = *reinterpret_cast<const float2 *>(betas + col);
-                    float y0[2] = {sgn * acc[nt][0] * bb.x, sgn * acc[nt][1] * bb.y};
-                    float y1[2] = {sgn * acc[nt][2] * bb.x, sgn * acc[nt][3] * bb.y};
-                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_TB + sw128_off(16 * ta + g, 2 * tb2 + nt) + 4 * t) =
-                        pack_bf16x2(y0[0], y0[1]);
-                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_TB + sw128_off(16 * ta + g + 8, 2 * tb2 + nt) + 4 * t) =
-                        pack_bf16x2(y1[0], y1[1]);
+                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_TB + sw128_off(16 * ta + g, 2 * tb + nt) + 4 * t) =
+                        pack_bf16x2(sgn * acc[nt][0] * bb.x, sgn * acc[nt][1] * bb.y);
+                    *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_TB + sw128_off(16 * ta + g + 8, 2 * tb + nt) + 4 * t) =
+                        pack_bf16x2(sgn * acc[nt][2] * bb.x, sgn * acc[nt][3] * bb.y);
+                }
+            };
+            {
+                // stage 1, (a, b) = (1,0) (2,1) (3,2) (2,0) (3,1) (3,0)
+                const int a = warp < 3 ? warp + 1 : (warp == 3 ? 2 : 3);
+                const int b = warp < 3 ? warp : (warp == 4 ? 1 : 0);
+                float acc[2][4] = {};
+                gemm16<false, true, true>(acc, LB(a, b), LST, LB(b, b), LST, lane);
+                store_c16(acc, XB(warp), XS, lane);
+            }
+            ut_sync();
+            {
+                // stage 2
+                float acc[2][4] = {};
+                if (warp < 3) {
+                    const int a = warp + 1;
+                    gemm16<false, true, false>(acc, LB(a, a), LST, XB(M10 + warp), XS, lane);
+                    tb_store(a, a - 1, -1.f, acc);
+                    if (warp == 2) {
+#pragma unroll
+                        for (int i = 0; i < 8; ++i) acc[i >> 2][i & 3] = -acc[i >> 2][i & 3];
+                        store_c16(acc, XB(T32F), XS, lane);
+                    }
+                } else {
+                    // V20 = M21 M10 - M20, V31 = M32 M21 - M31, Y30 = M31 M10 - M30
+                    const int left = warp == 3 ? M21 : (warp == 4 ? M32 : M31);
+                    const int right = warp == 4 ? M21 : M10;
+                    const int sub = warp == 3 ? M20 : (warp == 4 ? M31 : M30);
+                    load_c16(acc, XB(sub), XS, lane, -1.f);
+                    gemm16<false, false, false>(acc, XB(left), XS, XB(right), XS, lane);
+                    store_c16(acc, XB(V20 + (warp - 3)), XS, lane);
+                }
+            }
+            ut_sync();
+            if (warp >= 3) {
+                // stage 3
+                float acc[2][4] = {};
+                if (warp == 3) {
+                    gemm16<false, true, false>(acc, LB(2, 2), LST, XB(V20), XS, lane);
+                    tb_store(2, 0, 1.f, acc);
+                } else if (warp == 4) {
+                    gemm16<false, true, false>(acc, LB(3, 3), LST, XB(V31), XS, lane);
+                    tb_store(3, 1, 1.f, acc);
+                } else {
+                    gemm16<false, true, false>(acc, LB(3, 3), LST, XB(Y30), XS, lane);
+                    gemm16<false, false, false>(acc, XB(T32F), XS, XB(V20), XS, lane);
+                    tb_store(3, 0, 1.f, acc);
+                }
+            }
+        } else {
+            // warps 6..15, once the diagonal blocks are done: the previous chunk's
+            // outputs (D1 rows 64..127) and the bf16 copy of this chunk's incoming
+            // state (TMEM state, final since the previous chunk's last MMA) for this
+            // chunk's W S and Q+ S; then the zero parts of [Tb; 0]
+            diag_done_wait();
+            const int w6 = warp - 6;   // 0..9
+            if (w6 == 0 || w6 == 1) {
+                // warps 6 (lanes 64..95) and 7 (lanes 96..127): the previous chunk's
+                // outputs, one token row per lane, into the staging tile (the g tile
+                // is scanned), then out with two bulk tensor stores; the next g tile
+                // is loaded once the stores have read the staging tile
+                if (c > 0) {
+                    const int t = 32 * (sp - 2) + lane;
+#pragma unroll
+                    for (int q4 = 0; q4 < 4; ++q4) {
+                        float v32[32];
+                        tmem_ld32(tlane + TM_D1 + 32 * q4, v32);
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float x[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
+                            SM_U4(OFF_G + (q4 >> 1) * 8192 + sw128_off(t, 4 * (q4 & 1) + i)) = pack_bf16x8(x);
+                        }
+                    }
+                    fence_proxy_async();
+                }
+                asm volatile("bar.sync 3, 64;" ::: "memory");
+                if (tid == 192) {
+                    if (c > 0) {
+                        tma_store_2d(&maps.o, h * kD, (int32_t)(t0 - kC), sb + OFF_G);
+                        tma_store_2d(&maps.o, h * kD + 64, (int32_t)(t0 - kC), sb + OFF_G + 8192);
+                        bulk_commit();
+                        bulk_wait_read_all();
+                    }
+                    if (c + 1 < nchunks) {
+                        issue_g(t0 + kC);
+                        misc[2] = c + 1;
+                    }
+                }
+            } else if (c > 0) {
+                // warps 8..15: state rows 32 sp .. 32 sp + 31, 64 columns each
+                const int c64 = (w6 - 2) >> 2;          // column half
+                const int row = 32 * sp + lane;
+                const uint32_t sdst = OFF_S + c64 * 16384;
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float v32[32];
+                    tmem_ld32(tlane + TM_S + 64 * c64 + 32 * q2, v32);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        float x[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
+                        SM_U4(sdst + sw128_off(row, 4 * q2 + i)) = pack_bf16x8(x);
+                    }
+                }
+            }
+            // rows 64..127, and the blocks above the diagonal (row tile a, 16-byte
+            // chunks 2(a+1)..7)
+            const uint4 z = make_uint4(0, 0, 0, 0);
+            for (int i = tid - 192; i < 512 + 192; i += kThreads - 192) {
+                if (i < 512) {
+                    SM_U4(OFF_GR + GR_TB + sw128_off(64 + (i >> 3), i & 7)) = z;
+                } else {
+                    const int j = i - 512;
+                    const int row = j < 96 ? j / 6 : (j < 160 ? 16 + (j - 96) / 4 : 32 + (j - 160) / 2);
+                    const int ch = j < 96 ? 2 + j % 6 : (j < 160 ? 4 + (j - 96) % 4 : 6 + (j - 160) % 2);
+                    SM_U4(OFF_GR + GR_TB + sw128_off(row, ch)) = z;
                 }
             }
         }
@@ -631,6 +736,16 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
+        // while the tensor core works: S <- Diag(e^{G_63}) S in TMEM, so that the
+        // next MMA adds Khat^T U straight into the state
+        {
+            const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * srow);
+            float v32[32];
+            tmem_ld32(tlane + TM_S + 32 * qq, v32);
+#pragma unroll
+            for (int j = 0; j < 32; ++j) v32[j] *= dec;
+            tmem_st32(tlane + TM_S + 32 * qq, v32);
+        }
         wait_mma();
         // q of this chunk is consumed: prefetch the next chunk's
         if (tid == 0 && c + 1 < nchunks) {
@@ -655,7 +770,8 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- step 9: O = Q+ S + P U (D1 rows 64..127), D3 = Khat^T U
+        // ---------------- step 9: O = Q+ S + P U (D1 rows 64..127), S += Khat^T U.
+        // Not waited for here: the next chunk's loads and scan run meanwhile.
         if (tid == 0) {
             tc_fence_after();
             const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
@@ -664,56 +780,33 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = sw128_desc(gr + GR_U + kk * 2048, 8192, 1024);
                 mma_bf16(tmem + TM_D1, sw128_desc(gr + GR_P + kk * 32, 0, 1024), bd, id2, 1);
-                mma_bf16(tmem + TM_D3, sw128_desc(sb + kbuf + kk * 2048, 8192, 1024), bd, id3, kk > 0);
+                mma_bf16(tmem + TM_S, sw128_desc(sb + kbuf + kk * 2048, 8192, 1024), bd, id3, 1);
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
         if (tid < kC && c + 1 < nchunks)
             beta_next = (tid < eos - (t0 + kC)) ? beta[(size_t)(t0 + kC + tid) * H + h] : 0.f;
-        wait_mma();
-        // Khat is consumed: the next chunk's v goes into its buffer
-        if (tid == 0 && c + 1 < nchunks) {
-            issue_v(t0 + kC, kbuf);
-            issued[2] = c + 1;
-        }
+    }
 
-        // ---------------- step 10: outputs and the state update
-        {
-            if (sp >= 2) {
-                const int t = 32 * (sp - 2) + lane;
-                float v32[32];
-                tmem_ld32(tlane + TM_D1 + 32 * qq, v32);
-                if (t < lenc) {
-                    uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(t0 + t) * H + h) * kD + 32 * qq);
+    // the last chunk: its outputs once its last MMAs are done
+    if (!misc[1] && nchunks > 0) {
+        wait_mma();
+        if (sp >= 2) {
+            const int64_t tl = bos + (int64_t)(nchunks - 1) * kC;
+            const int t = 32 * (sp - 2) + lane;
+            float v32[32];
+            tmem_ld32(tlane + TM_D1 + 32 * qq, v32);
+            if (tl + t < eos) {
+                uint4 *dst = reinterpret_cast<uint4 *>(out + ((size_t)(tl + t) * H + h) * kD + 32 * qq);
 #pragma unroll
-                    for (int i = 0; i < 4; ++i) {
-                        float x[8];
+                for (int i = 0; i < 4; ++i) {
+                    float x[8];
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
-                        dst[i] = pack_bf16x8(x);
-                    }
+                    for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
+                    dst[i] = pack_bf16x8(x);
                 }
             }
-            const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * srow);
-            float ds[64];    // [D3 | S]
-            tmem_wait_st();  // the previous chunk's store of S has landed
-            tmem_ld32x2(tlane + TM_D3 + 32 * qq, tlane + TM_S + 32 * qq, ds);
-            float S[32];
-#pragma unroll
-            for (int j = 0; j < 32; ++j) S[j] = dec * ds[32 + j] + ds[j];
-            tmem_st32_nowait(tlane + TM_S + 32 * qq, S);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = S[8 * i + e];
-                SM_U4(s_smem + sw128_off(srow, 4 * (qq & 1) + i)) = pack_bf16x8(x);
-            }
         }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-        if (misc[1]) break;
     }
 
     if (misc[1]) {
@@ -721,6 +814,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         if (tid == 0) {
             flag_status(status, KDA_DEVICE_TIMEOUT);
             mbar_wait(sb + OFF_BAR + BAR_MMA, mma_phase, 100000000ull);
+            issued[3] = (int)misc[2];   // the g tiles are loaded by thread 192
             const uint32_t bars[4] = {BAR_Q, BAR_K, BAR_V, BAR_G};
             for (int i = 0; i < 4; ++i)
                 if (issued[i] >= c)   // issued for this chunk or the next, maybe not landed
@@ -728,7 +822,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         }
     } else if (final_state != nullptr) {
         tc_fence_after();
-        tmem_wait_st();
         float S[32];
         tmem_ld32(tlane + TM_S + 32 * qq, S);
         float *dst = final_state + unit * kD * kD + (size_t)srow * kD + 32 * qq;
@@ -736,6 +829,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         for (int j = 0; j < 32; j += 4)
             *reinterpret_cast<float4 *>(dst + j) = make_float4(S[j], S[j + 1], S[j + 2], S[j + 3]);
     }
+    if (tid == 192) bulk_wait_all();   // the output stores of thread 192 are complete
     tmem_wait_st();
     tc_fence_before();
     __syncthreads();
@@ -795,7 +889,8 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  cudaStream_t stream) {
     Maps maps;
     if (!make_map(&maps.q, q, T, H, false) || !make_map(&maps.k, k, T, H, false) ||
-        !make_map(&maps.v, v, T, H, false) || !make_map(&maps.g, g, T, H, true))
+        !make_map(&maps.v, v, T, H, false) || !make_map(&maps.g, g, T, H, true) ||
+        !make_map(&maps.o, out, T, H, false))
         return cudaErrorInvalidValue;
     static bool attr_set = false;
     if (!attr_set) {
