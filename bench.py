@@ -93,13 +93,14 @@ class Dist:
 # ------------------------------------------------------------------ clocks
 
 class ClockSampler:
-    """nvidia-smi samples (200 ms) while GPU work runs."""
+    """nvidia-smi samples (every 50 ms) while GPU work runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, interval_ms: int = 50):
         self.gpu = gpu_index
+        self.interval = interval_ms
         self.proc = None
         self.path = None
 
@@ -110,7 +111,7 @@ class ClockSampler:
             self.out = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.gpu)], stdout=self.out,
+                 "-lms", str(self.interval), "-i", str(self.gpu)], stdout=self.out,
                 stderr=subprocess.DEVNULL)
         except OSError:
             self.proc = None
@@ -189,6 +190,12 @@ def traffic_for(kernel, units):
         return int(entry["dram_bytes"] * units / entry["units"])
     except (OSError, KeyError, ValueError):
         return None
+
+
+def prologue_traffic(T):
+    """DRAM bytes of the two prologue kernels together (conv and gates)."""
+    a, b = traffic_for("conv_swish_norm_kernel", T), traffic_for("gates_kernel", T)
+    return None if a is None or b is None else a + b
 
 
 def roofline(bytes_per_launch, launch_ms, peak_gbs, traffic=None):
@@ -325,7 +332,7 @@ def bench_long(kda, dist, args, peaks):
                     "once (the fused minimum); the prologue and the prefill run as two kernels",
             "prologue": {"ms": round(pro, 3),
                          "roofline": roofline(PROLOGUE_BYTES_PER_TOKEN * T + conv_w.numel() * 4,
-                                              pro, peaks["hbm_gbs"])},
+                                              pro, peaks["hbm_gbs"], prologue_traffic(T))},
             "prefill": {"ms": round(pre, 3),
                         "roofline": roofline(BYTES_PER_TOKEN * T + STATE_BYTES, pre,
                                              peaks["hbm_gbs"], traffic_for("chunk_kernel", T))}}
@@ -482,15 +489,24 @@ def main():
             print(json.dumps({"only": args.only, "result": res}), flush=True)
         dist.close()
         return 0
-    clocks = ClockSampler(dist.local)
-    clocks.start()
-    pre = bench_prefill(kda, synth, dist, args, peaks)
-    dec = None if args.no_decode else bench_decode(kda, synth, dist, args, peaks)
+    # the headline's clock record covers the prefill leg only; every other leg
+    # carries its own
+    def sampled(fn):
+        sampler = ClockSampler(dist.local)
+        sampler.start()
+        res = fn()
+        clk_leg = sampler.stop()
+        if isinstance(res, dict):
+            res["clocks"] = clk_leg
+        return res, clk_leg
+
+    pre, clk = sampled(lambda: bench_prefill(kda, synth, dist, args, peaks))
+    pre.pop("clocks", None)
+    dec = None if args.no_decode else sampled(lambda: bench_decode(kda, synth, dist, args, peaks))[0]
     torch.cuda.empty_cache()
-    lng = None if args.no_long else bench_long(kda, dist, args, peaks)
+    lng = None if args.no_long else sampled(lambda: bench_long(kda, dist, args, peaks))[0]
     torch.cuda.empty_cache()
-    ext = bench_extras(kda, dist, args, peaks)
-    clk = clocks.stop()
+    ext = sampled(lambda: bench_extras(kda, dist, args, peaks))[0]
     cb = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(synth, H)
