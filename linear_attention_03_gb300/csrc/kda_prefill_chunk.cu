@@ -89,11 +89,14 @@ constexpr uint32_t VEC_SEG = 0;         // fp32 [8][128]  sums of g over the 8-t
 constexpr uint32_t VEC_DEC = 4096;      // fp32 [128]     e^{G_63} of the chunk
 constexpr uint32_t OFF_BETA = OFF_VEC + 4608;       // [64] fp32
 constexpr uint32_t OFF_BAR = OFF_BETA + 256;        // mbarriers
-constexpr uint32_t OFF_MISC = OFF_BAR + 64;         // tmem base, abort flag, last g chunk loaded
-constexpr uint32_t SMEM_USED = OFF_MISC + 16;
+// tmem base, abort flag, then the chunk index of the last g, v, k, q load issued
+constexpr uint32_t OFF_MISC = OFF_BAR + 64;
+constexpr uint32_t SMEM_USED = OFF_MISC + 32;
 constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 
 constexpr uint32_t BAR_Q = 0, BAR_K = 8, BAR_V = 16, BAR_G = 24, BAR_MMA = 32;
+// a chunk's last two MMA groups are issued by two threads, each committing here
+constexpr uint32_t BAR_MMA2 = 40;
 
 // TMEM columns
 constexpr uint32_t TM_D1 = 0;     // [U ; O] accumulator
@@ -218,8 +221,9 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(sb + OFF_BAR + 8 * i, 1);
+        mbar_init(sb + OFF_BAR + BAR_MMA2, 2);
         misc[1] = 0;
-        misc[2] = 0;
+        for (int i = 2; i < 6; ++i) misc[i] = 0;
         fence_mbar_init();
     }
     if (warp == 0) tmem_alloc(sb + OFF_MISC, TM_COLS);
@@ -277,25 +281,29 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         tma_load_2d(sb + OFF_G, &maps.g, h * kD, (int32_t)t0, sb + OFF_BAR + BAR_G);
     };
 
-    // chunk index of the last load issued on each TMA barrier (thread 0 only),
-    // so an aborting CTA can drain its own copies before it exits
-    int issued[4] = {-1, -1, -1, -1};
+    // the loads are issued by threads of different warps (a TMA issue holds its
+    // thread for a while); each records the chunk index in misc[2..5] (g, v, k,
+    // q) so an aborting CTA can drain its own copies before it exits
     if (tid == 0 && nchunks > 0) {
         issue_q(bos);
         issue_k(bos, buf_off(0));
         issue_v(bos, buf_off(1));
         issue_g(bos);
-        issued[0] = issued[1] = issued[2] = issued[3] = 0;
     }
     // beta of the next chunk, held in a register by threads 0..63
     float beta_next = 0.f;
     if (tid < kC && nchunks > 0 && tid < len) beta_next = beta[(size_t)(bos + tid) * H + h];
 
-    uint32_t mma_phase = 0;
+    uint32_t mma_phase = 0, mma2_phase = 0;
     // all threads wait on the MMA barrier; a timeout raises the abort flag
     auto wait_mma = [&]() {
         if (!mbar_wait(sb + OFF_BAR + BAR_MMA, mma_phase)) misc[1] = 1;
         mma_phase ^= 1;
+        tc_fence_after();
+    };
+    auto wait_mma2 = [&]() {
+        if (!mbar_wait(sb + OFF_BAR + BAR_MMA2, mma2_phase)) misc[1] = 1;
+        mma2_phase ^= 1;
         tc_fence_after();
     };
     auto wait_tma = [&](uint32_t bar, int c) {
@@ -344,24 +352,12 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             __syncthreads();
             // the previous chunk's last MMAs (O += P U, S += Khat^T U) have run
             // while this chunk loaded and scanned: its P, U and Khat are free now
-            if (c > 0) wait_mma();
-            if (tid == 0) {
-                // the chunk after the next one: into L2 now, so that its loads hit L2
-                if (c + 2 < nchunks) {
-                    const int32_t y2 = (int32_t)(t0 + 2 * kC);
-                    tma_prefetch_2d(&maps.q, h * kD, y2);
-                    tma_prefetch_2d(&maps.q, h * kD + 64, y2);
-                    tma_prefetch_2d(&maps.k, h * kD, y2);
-                    tma_prefetch_2d(&maps.k, h * kD + 64, y2);
-                    tma_prefetch_2d(&maps.v, h * kD, y2);
-                    tma_prefetch_2d(&maps.v, h * kD + 64, y2);
-                    tma_prefetch_2d(&maps.g, h * kD, y2);
-                }
-                // this chunk's v goes into the buffer that held the previous Khat
-                if (c > 0) {
-                    issue_v(t0, vbuf);
-                    issued[2] = c;
-                }
+            if (c > 0) wait_mma2();
+            // this chunk's v goes into the buffer that held the previous Khat (warp
+            // 15 writes the fewest Gram rows in the pass below)
+            if (tid == 480 && c > 0) {
+                issue_v(t0, vbuf);
+                misc[3] = c;
             }
             // segment boundaries (log2 units), as predicated running sums so that no
             // array is indexed at run time: G before this segment, before tile a
@@ -702,10 +698,11 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
         wait_mma();
-        // v is consumed: the next chunk's k goes into its buffer
-        if (tid == 0 && c + 1 < nchunks) {
+        // v is consumed: the next chunk's k goes into its buffer (warp 14 has no
+        // part in the -W read below)
+        if (tid == 448 && c + 1 < nchunks) {
             issue_k(t0 + kC, vbuf);
-            issued[1] = c + 1;
+            misc[4] = c + 1;
         }
         // -W -> rows 0..63 of A1 (warps of sub-partitions 0 and 1)
         if (sp < 2) {
@@ -747,10 +744,11 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             tmem_st32(tlane + TM_S + 32 * qq, v32);
         }
         wait_mma();
-        // q of this chunk is consumed: prefetch the next chunk's
-        if (tid == 0 && c + 1 < nchunks) {
+        // q of this chunk is consumed: load the next chunk's (warp 15 has no part
+        // in the U read below)
+        if (tid == 480 && c + 1 < nchunks) {
             issue_q(t0 + kC);
-            issued[0] = c + 1;
+            misc[5] = c + 1;
         }
 
         // ---------------- step 8: U (D1 rows 0..63) -> bf16 MN-major B operand
@@ -772,17 +770,19 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 
         // ---------------- step 9: O = Q+ S + P U (D1 rows 64..127), S += Khat^T U.
         // Not waited for here: the next chunk's loads and scan run meanwhile.
-        if (tid == 0) {
+        // Two issuing threads (warps 0 and 1), one per accumulator.
+        if (tid == 0 || tid == 32) {
             tc_fence_after();
-            const uint32_t id2 = idesc_bf16(128, 128, 0, 1);
-            const uint32_t id3 = idesc_bf16(128, 128, 1, 1);
+            const bool o_part = tid == 0;
+            const uint32_t id = o_part ? idesc_bf16(128, 128, 0, 1) : idesc_bf16(128, 128, 1, 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t bd = sw128_desc(gr + GR_U + kk * 2048, 8192, 1024);
-                mma_bf16(tmem + TM_D1, sw128_desc(gr + GR_P + kk * 32, 0, 1024), bd, id2, 1);
-                mma_bf16(tmem + TM_S, sw128_desc(sb + kbuf + kk * 2048, 8192, 1024), bd, id3, 1);
+                const uint64_t ad = o_part ? sw128_desc(gr + GR_P + kk * 32, 0, 1024)
+                                           : sw128_desc(sb + kbuf + kk * 2048, 8192, 1024);
+                mma_bf16(tmem + (o_part ? TM_D1 : TM_S), ad, bd, id, 1);
             }
-            mma_commit(sb + OFF_BAR + BAR_MMA);
+            mma_commit(sb + OFF_BAR + BAR_MMA2);
         }
         if (tid < kC && c + 1 < nchunks)
             beta_next = (tid < eos - (t0 + kC)) ? beta[(size_t)(t0 + kC + tid) * H + h] : 0.f;
@@ -790,7 +790,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
 
     // the last chunk: its outputs once its last MMAs are done
     if (!misc[1] && nchunks > 0) {
-        wait_mma();
+        wait_mma2();
         if (sp >= 2) {
             const int64_t tl = bos + (int64_t)(nchunks - 1) * kC;
             const int t = 32 * (sp - 2) + lane;
@@ -814,7 +814,8 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         if (tid == 0) {
             flag_status(status, KDA_DEVICE_TIMEOUT);
             mbar_wait(sb + OFF_BAR + BAR_MMA, mma_phase, 100000000ull);
-            issued[3] = (int)misc[2];   // the g tiles are loaded by thread 192
+            mbar_wait(sb + OFF_BAR + BAR_MMA2, mma2_phase, 100000000ull);
+            const int issued[4] = {(int)misc[5], (int)misc[4], (int)misc[3], (int)misc[2]};
             const uint32_t bars[4] = {BAR_Q, BAR_K, BAR_V, BAR_G};
             for (int i = 0; i < 4; ++i)
                 if (issued[i] >= c)   // issued for this chunk or the next, maybe not landed
