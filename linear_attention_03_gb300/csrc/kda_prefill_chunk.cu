@@ -112,17 +112,16 @@ struct Maps {
     CUtensorMap q, k, v, g, o;
 };
 
-// ---- 16x16x16 fp32 products for the block inverse, one warp each, on the
+// ---- 16x16x16 products for the block inverse, one warp each, on the
 // warp-synchronous tensor-core path (mma.sync m16n8k8, tf32 in, fp32 out).
-// Every operand is split into two tf32 terms (x = hi + lo) and the three
-// significant cross products are accumulated, which keeps fp32-level accuracy.
-// Fragment layout (g = lane / 4, t = lane % 4): A rows g and g+8, columns t
-// and t+4 of each 8-wide K slice; B K-rows t and t+4, column g; D rows g and
-// g+8, columns 2t and 2t+1 of each 8-wide N tile.
-__device__ __forceinline__ void tf32_split(float x, uint32_t &hi, uint32_t &lo) {
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(hi) : "f"(x));
-    const float r = x - __uint_as_float(hi);
-    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(lo) : "f"(r));
+// Operands are rounded to tf32 (10-bit mantissa, 3 bits more than the bf16
+// Tb they produce).  Fragment layout (g = lane / 4, t = lane % 4): A rows g
+// and g+8, columns t and t+4 of each 8-wide K slice; B K-rows t and t+4,
+// column g; D rows g and g+8, columns 2t and 2t+1 of each 8-wide N tile.
+__device__ __forceinline__ uint32_t to_tf32(float x) {
+    uint32_t r;
+    asm("cvt.rna.tf32.f32 %0, %1;" : "=r"(r) : "f"(x));
+    return r;
 }
 __device__ __forceinline__ void mma_tf32(float (&d)[4], const uint32_t (&a)[4], const uint32_t (&b)[2]) {
     asm volatile(
@@ -139,31 +138,19 @@ __device__ __forceinline__ void gemm16(float (&acc)[2][4], const float *A, int s
     const int g = lane >> 2, t = lane & 3;
     auto Ael = [&](int r, int k) { return AT ? A[k * sa + r] : A[r * sa + k]; };
     auto Bel = [&](int k, int n) { return BT ? B[n * sb + k] : B[k * sb + n]; };
-    // the three cross products go to separate accumulators, so that no MMA waits
-    // on the previous one's result for more than the two K slices
-    float p[3][2][4] = {};
 #pragma unroll
     for (int ks = 0; ks < 2; ++ks) {
         const float av[4] = {Ael(g, 8 * ks + t), Ael(g + 8, 8 * ks + t), Ael(g, 8 * ks + t + 4),
                              Ael(g + 8, 8 * ks + t + 4)};
-        uint32_t ah[4], al[4];
+        uint32_t a[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) tf32_split(NEG ? -av[i] : av[i], ah[i], al[i]);
+        for (int i = 0; i < 4; ++i) a[i] = to_tf32(NEG ? -av[i] : av[i]);
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt) {
-            const float bv[2] = {Bel(8 * ks + t, 8 * nt + g), Bel(8 * ks + t + 4, 8 * nt + g)};
-            uint32_t bh[2], bl[2];
-            tf32_split(bv[0], bh[0], bl[0]);
-            tf32_split(bv[1], bh[1], bl[1]);
-            mma_tf32(p[0][nt], ah, bh);
-            mma_tf32(p[1][nt], ah, bl);
-            mma_tf32(p[2][nt], al, bh);
+            const uint32_t b[2] = {to_tf32(Bel(8 * ks + t, 8 * nt + g)), to_tf32(Bel(8 * ks + t + 4, 8 * nt + g))};
+            mma_tf32(acc[nt], a, b);
         }
     }
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-        for (int i = 0; i < 4; ++i) acc[nt][i] += (p[2][nt][i] + p[1][nt][i]) + p[0][nt][i];
 }
 // D-layout fragments from / to a row-major 16x16 fp32 block (row stride sc)
 __device__ __forceinline__ void load_c16(float (&acc)[2][4], const float *C, int sc, int lane, float scale) {
