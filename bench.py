@@ -399,6 +399,38 @@ def bench_extras(kda, dist, args, peaks):
                           "value": round(T * args.steps / (total * 1e-3), 1), "unit": "tokens/s",
                           "roofline": roofline(GATE_BYTES * T * H, statistics.mean(per),
                                                peaks["hbm_gbs"])}
+    del o, z, y
+    # segmented prefill of one long document: with few heads the plain prefill
+    # fills only H SMs; the segments give segments x H CTAs at 3x the arithmetic
+    for Hs, nseg in ((8, 16), (96, 2)):
+        T = 65536
+        q = torch.nn.functional.normalize(rnd(T, Hs, D), dim=-1).to(torch.bfloat16)
+        k = torch.nn.functional.normalize(rnd(T, Hs, D), dim=-1).to(torch.bfloat16)
+        v = rnd(T, Hs, D, dt=torch.bfloat16)
+        g = -5.0 * torch.sigmoid(rnd(T, Hs, D))
+        b = torch.sigmoid(rnd(T, Hs))
+        o3 = torch.empty_like(v)
+        fin = torch.empty(Hs, D, D, device="cuda")
+        ws = torch.empty(kda.kda_prefill_segmented_workspace_size(Hs, D, torch.bfloat16, T, nseg),
+                         dtype=torch.uint8, device="cuda")
+        ws1 = torch.empty(kda.kda_prefill_workspace_size(Hs, D, torch.bfloat16, T, 1),
+                          dtype=torch.uint8, device="cuda")
+        fin1 = torch.empty(1, Hs, D, D, device="cuda")
+        seg = lambda: kda.kda_prefill_segmented(q, k, v, g, b, None, nseg, out=o3, final_state=fin,
+                                                workspace=ws)
+        plain = lambda: kda.kda_prefill(q, k, v, g, b, None, None, out=o3, final_state=fin1,
+                                        workspace=ws1)
+        steps = max(1, min(args.steps, 5))
+        t_seg, _ = time_steps(dist, seg, steps, min(args.warmup, 2))
+        t_plain, _ = time_steps(dist, plain, steps, min(args.warmup, 2))
+        bytes_step = BYTES_PER_TOKEN // H * Hs * T + Hs * D * D * 4
+        res[f"segmented_h{Hs}"] = {
+            "workload": f"one document T={T}, H={Hs}, d=128 bf16, {nseg} segments",
+            "value": round(T * steps / (t_seg * 1e-3), 1), "unit": "tokens/s",
+            "plain_prefill_tokens_per_s": round(T * steps / (t_plain * 1e-3), 1),
+            "speedup_vs_plain": round(t_plain / t_seg, 3),
+            "roofline": roofline(bytes_step, t_seg / steps, peaks["hbm_gbs"])}
+        del q, k, v, g, b, o3, ws
     return res
 
 

@@ -119,6 +119,38 @@ KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v,
                        size_t workspace_bytes, void *stream);
 
 /*
+ * Bytes of device workspace kda_prefill_segmented needs (0 for invalid
+ * arguments).  It holds the status word, the segment offsets, a zero value
+ * tile, five [segments, H, d_k, d_v] fp32 state sets and one [T, H, d_v]
+ * output tile.
+ */
+KDA_API size_t kda_prefill_segmented_workspace_size(kda_dims dims, int64_t T, int32_t num_segments);
+
+/*
+ * Prefill of ONE document of T tokens split into num_segments segments that
+ * run as independent documents (for long documents whose heads alone cannot
+ * fill the GPU).  Over a segment the state evolves affinely, S_out = P S_in +
+ * R, and such maps compose by (P2, R2) o (P1, R1) = (P2 P1, P2 R1 + R2)
+ * ("From GPT-2 to Kimi K3, from first principles", Chapter 6, context
+ * parallelism).  R comes from a prefill from zero with v, P from a prefill
+ * from the identity with v = 0, a scan joins the segments, and a prefill from
+ * each segment's incoming state with v = 0 gives the outputs that state adds.
+ * The result equals kda_prefill of the document (up to rounding) at three
+ * times its arithmetic.
+ *   q, k, g  [T, H, d_k];  v, out [T, H, d_v];  beta [T, H]  (as kda_prefill)
+ *   init_state, final_state [H, d_k, d_v] fp32 or NULL; final_state may alias
+ *   num_segments >= 1; segments are whole 64-token chunks, the last may be
+ *   shorter, and fewer segments than asked are used when T is short
+ *   workspace  kda_prefill_segmented_workspace_size() bytes, 256-byte
+ *              aligned; its first word is the device status word
+ */
+KDA_API kda_status kda_prefill_segmented(const void *q, const void *k, const void *v,
+                                         const float *g, const float *beta,
+                                         const float *init_state, int64_t T, kda_dims dims,
+                                         int32_t num_segments, void *out, float *final_state,
+                                         void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * One decode step for N independent sequences, one token each
  * ("fused_recurrent" mode of "From GPT-2 to Kimi K3", Chapter 6).  Reads
  * every fp32 state once and writes it back in place.

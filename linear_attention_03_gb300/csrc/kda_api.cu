@@ -137,6 +137,53 @@ kda_status kda_prefill(const void *q, const void *k, const void *v,
     return KDA_OK;
 }
 
+size_t kda_prefill_segmented_workspace_size(kda_dims dims, int64_t T, int32_t num_segments) {
+    if (check_dims(dims) != KDA_OK || T < 0 || num_segments < 1) return 0;
+    return kda::segmented_workspace_size(dims.H, dims.d_k, (kda_dtype)dims.qkv_dtype, T, num_segments);
+}
+
+kda_status kda_prefill_segmented(const void *q, const void *k, const void *v, const float *g,
+                                 const float *beta, const float *init_state, int64_t T,
+                                 kda_dims dims, int32_t num_segments, void *out,
+                                 float *final_state, void *workspace, size_t workspace_bytes,
+                                 void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (T < 0 || T > INT32_MAX) return fail(KDA_ERR_INVALID, "T must be in [0, 2^31)%s");
+    if (num_segments < 1 || num_segments > 65535)
+        return fail(KDA_ERR_INVALID, "num_segments must be in [1, 65535]%s");
+    if (T > 0) {
+        KDA_TRY(need(q, "q"));
+        KDA_TRY(need(k, "k"));
+        KDA_TRY(need(v, "v"));
+        KDA_TRY(need(g, "g"));
+        KDA_TRY(need4(beta, "beta"));
+        KDA_TRY(need(out, "out"));
+    }
+    KDA_TRY(maybe(init_state, "init_state"));
+    KDA_TRY(maybe(final_state, "final_state"));
+    KDA_TRY(need(workspace, "workspace"));
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(KDA_ERR_INVALID, "workspace must be 256-byte aligned%s");
+    if (workspace_bytes < kda_prefill_segmented_workspace_size(dims, T, num_segments))
+        return fail(KDA_ERR_INVALID, "workspace too small (see kda_prefill_segmented_workspace_size)%s");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        cudaError_t err = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+        const size_t bytes = (size_t)dims.H * dims.d_k * dims.d_v * sizeof(float);
+        if (err == cudaSuccess && final_state != nullptr && final_state != init_state)
+            err = init_state ? cudaMemcpyAsync(final_state, init_state, bytes, cudaMemcpyDeviceToDevice, s)
+                             : cudaMemsetAsync(final_state, 0, bytes, s);
+        return err == cudaSuccess ? KDA_OK : cuda_fail(err, "segmented prefill (T = 0)");
+    }
+    const kda_dtype dt = (kda_dtype)dims.qkv_dtype;
+    const bool chunk = kda::chunk_prefill_supported(dims.d_k, dt) && !force_recurrent();
+    cudaError_t err = kda::launch_prefill_segmented(q, k, v, g, beta, init_state, T, dims.H, dims.d_k, dt,
+                                                    num_segments, out, final_state, workspace, chunk, s);
+    if (err != cudaSuccess) return cuda_fail(err, "segmented prefill launch");
+    return KDA_OK;
+}
+
 kda_status kda_decode_step(const void *q, const void *k, const void *v,
                            const float *g, const float *beta, float *state,
                            void *out, int32_t N, kda_dims dims, void *stream) {

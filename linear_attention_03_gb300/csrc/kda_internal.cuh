@@ -132,4 +132,12 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  void *out, float *final_state, int32_t *status,
                                  cudaStream_t stream);
 
+// prefill of one document as independent segments joined by an exact scan
+size_t segmented_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int32_t num_segments);
+cudaError_t launch_prefill_segmented(const void *q, const void *k, const void *v, const float *g,
+                                     const float *beta, const float *init_state, int64_t T, int32_t H,
+                                     int32_t D, kda_dtype dt, int32_t num_segments, void *out,
+                                     float *final_state, void *workspace, bool use_chunk,
+                                     cudaStream_t s);
+
 }  // namespace kda

@@ -28,7 +28,8 @@ KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT = 0, 1, 2
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
            "kda_prologue", "kda_get_device_status", "kda_last_error",
            "kda_kernel_launches", "kda_decode_step_conv", "kda_decode_verify",
-           "kda_output_gate", "kda_prefill_noalloc", "kda_selftest_wait")
+           "kda_output_gate", "kda_prefill_noalloc", "kda_selftest_wait",
+           "kda_prefill_segmented_workspace_size", "kda_prefill_segmented")
 
 
 class kda_dims(ctypes.Structure):
@@ -41,6 +42,10 @@ lib.kda_prefill_workspace_size.argtypes = [kda_dims, _i64, _i32]
 lib.kda_prefill_workspace_size.restype = _sz
 lib.kda_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
                             _sz, _P]
+lib.kda_prefill_segmented_workspace_size.argtypes = [kda_dims, _i64, _i32]
+lib.kda_prefill_segmented_workspace_size.restype = _sz
+lib.kda_prefill_segmented.argtypes = [_P, _P, _P, _P, _P, _P, _i64, kda_dims, _i32, _P, _P, _P,
+                                      _sz, _P]
 lib.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
 lib.kda_prologue.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
                              _P, _P, _P]
@@ -54,7 +59,8 @@ lib.kda_last_error.argtypes = []
 lib.kda_last_error.restype = ctypes.c_char_p
 lib.kda_kernel_launches.argtypes = []
 lib.kda_kernel_launches.restype = ctypes.c_uint64
-for _fn in (lib.kda_prefill, lib.kda_decode_step, lib.kda_prologue, lib.kda_get_device_status,
+for _fn in (lib.kda_prefill, lib.kda_prefill_segmented, lib.kda_decode_step, lib.kda_prologue,
+            lib.kda_get_device_status,
             lib.kda_decode_step_conv, lib.kda_decode_verify, lib.kda_output_gate):
     _fn.restype = ctypes.c_int
 
@@ -144,6 +150,43 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
                          _ptr(workspace), workspace.numel(), _stream())
     if st != KDA_OK:
         raise KDAError(st, "kda_prefill")
+    return out, final_state
+
+
+def kda_prefill_segmented_workspace_size(H: int, d: int, dtype: torch.dtype, T: int,
+                                         num_segments: int) -> int:
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib.kda_prefill_segmented_workspace_size(kda_dims(H, d, d, code), T, num_segments))
+
+
+def kda_prefill_segmented(q, k, v, g, beta, init_state=None, num_segments=2, out=None,
+                          final_state=None, workspace=None):
+    """One document as `num_segments` segments joined by an exact scan of their
+    affine state maps; returns (out, final_state [H, d, d])."""
+    T, H, d = q.shape
+    dev = q.device
+    _dev(q, "q")
+    _dev(k, "k", q.dtype, q.shape)
+    _dev(v, "v", q.dtype, q.shape)
+    _dev(g, "g", torch.float32, q.shape)
+    _dev(beta, "beta", torch.float32, (T, H))
+    _dev(init_state, "init_state", torch.float32, (H, d, d))
+    if out is None:
+        out = torch.empty_like(v)
+    _dev(out, "out", q.dtype, q.shape)
+    if final_state is None:
+        final_state = torch.empty((H, d, d), dtype=torch.float32, device=dev)
+    _dev(final_state, "final_state", torch.float32, (H, d, d))
+    dims = dims_of(q)
+    ws_bytes = int(lib.kda_prefill_segmented_workspace_size(dims, T, num_segments))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _dev(workspace, "workspace", torch.uint8)
+    st = lib.kda_prefill_segmented(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   _ptr(init_state), T, dims, num_segments, _ptr(out),
+                                   _ptr(final_state), _ptr(workspace), workspace.numel(), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prefill_segmented")
     return out, final_state
 
 

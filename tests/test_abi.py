@@ -88,6 +88,22 @@ def test_prefill_argument_checks(kda):
     assert call(wsb=ws - 1) == kda.KDA_ERR_INVALID
 
 
+def test_segmented_prefill_argument_checks(kda):
+    p = ctypes.c_void_p(FAKE)
+    d = dims(kda)
+    ws = kda.lib.kda_prefill_segmented_workspace_size(d, 4096, 4)
+    assert ws > 4096 * 4 * 128 * 2                       # holds the zero value tile
+    assert kda.lib.kda_prefill_segmented_workspace_size(d, 4096, 0) == 0
+    call = lambda **o: kda.lib.kda_prefill_segmented(
+        o.get("q", p), p, p, p, p, None, o.get("T", 4096), d, o.get("nseg", 4), p, None,
+        o.get("ws", p), o.get("wsb", ws), None)
+    assert call(nseg=0) == kda.KDA_ERR_INVALID and "num_segments" in kda.kda_last_error()
+    assert call(q=None) == kda.KDA_ERR_INVALID
+    assert call(ws=ctypes.c_void_p(FAKE + 16)) == kda.KDA_ERR_INVALID   # 256-byte alignment
+    assert call(wsb=ws - 1) == kda.KDA_ERR_INVALID
+    assert call(T=-1) == kda.KDA_ERR_INVALID
+
+
 def test_prologue_argument_checks(kda):
     p = ctypes.c_void_p(FAKE)
     d = dims(kda)
