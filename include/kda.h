@@ -119,6 +119,37 @@ KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v,
                        size_t workspace_bytes, void *stream);
 
 /*
+ * Bytes of device workspace kda_prologue_prefill needs (0 for invalid
+ * arguments): the status word, two segment-sized sets of q, k, v, g, beta and
+ * the running [H, d_k, d_v] fp32 state.
+ */
+KDA_API size_t kda_prologue_prefill_workspace_size(kda_dims dims, int64_t T, int64_t segment_tokens);
+
+/*
+ * The KDA input path and recurrence of ONE document from the raw projections
+ * ("An infra-oriented diagram of Kimi K3", KDA card: ShortConv, Swish, L2Norm,
+ * the scaled-sigmoid decay and the sigmoid beta; then the chunked prefill of
+ * "From GPT-2 to Kimi K3", Chapter 6), segment by segment: the prologue of
+ * the next segment overlaps the prefill of the current one, and the fp32
+ * state is carried across segments.  Equal (up to rounding) to kda_prologue
+ * followed by kda_prefill, without T-sized intermediates.
+ *   q_raw, k_raw, v_raw [T, H, d]  qkv_dtype;  conv_w [3, H*d, 4] fp32
+ *   z_g [T, H, d_k] fp32;  z_beta [T, H] fp32   (both required)
+ *   init_state, final_state [H, d_k, d_v] fp32 or NULL; final_state may alias
+ *   segment_tokens  tokens per segment (rounded up to a multiple of 64)
+ *   out [T, H, d_v] qkv_dtype
+ *   workspace  kda_prologue_prefill_workspace_size() bytes, 256-byte aligned;
+ *              its first word is the device status word
+ * The work runs on two library streams of the current device, after the work
+ * already queued on `stream`, and `stream` waits for it.
+ */
+KDA_API kda_status kda_prologue_prefill(const void *q_raw, const void *k_raw, const void *v_raw,
+                                        const float *conv_w, const float *z_g, const float *z_beta,
+                                        const float *init_state, int64_t T, kda_dims dims,
+                                        int64_t segment_tokens, void *out, float *final_state,
+                                        void *workspace, size_t workspace_bytes, void *stream);
+
+/*
  * Bytes of device workspace kda_prefill_segmented needs (0 for invalid
  * arguments).  It holds the status word, the segment offsets, a zero value
  * tile, five [segments, H, d_k, d_v] fp32 state sets and one [T, H, d_v]

@@ -137,6 +137,54 @@ kda_status kda_prefill(const void *q, const void *k, const void *v,
     return KDA_OK;
 }
 
+size_t kda_prologue_prefill_workspace_size(kda_dims dims, int64_t T, int64_t segment_tokens) {
+    if (check_dims(dims) != KDA_OK || T < 0 || segment_tokens < 1) return 0;
+    return kda::pipeline_workspace_size(dims.H, dims.d_k, (kda_dtype)dims.qkv_dtype, T, segment_tokens);
+}
+
+kda_status kda_prologue_prefill(const void *q_raw, const void *k_raw, const void *v_raw,
+                                const float *conv_w, const float *z_g, const float *z_beta,
+                                const float *init_state, int64_t T, kda_dims dims,
+                                int64_t segment_tokens, void *out, float *final_state,
+                                void *workspace, size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    KDA_TRY(check_dims(dims));
+    if (T < 0 || T > INT32_MAX) return fail(KDA_ERR_INVALID, "T must be in [0, 2^31)%s");
+    if (segment_tokens < 1) return fail(KDA_ERR_INVALID, "segment_tokens must be >= 1%s");
+    if (T > 0) {
+        KDA_TRY(need(q_raw, "q_raw"));
+        KDA_TRY(need(k_raw, "k_raw"));
+        KDA_TRY(need(v_raw, "v_raw"));
+        KDA_TRY(need(conv_w, "conv_w"));
+        KDA_TRY(need(z_g, "z_g"));
+        KDA_TRY(need4(z_beta, "z_beta"));
+        KDA_TRY(need(out, "out"));
+    }
+    KDA_TRY(maybe(init_state, "init_state"));
+    KDA_TRY(maybe(final_state, "final_state"));
+    KDA_TRY(need(workspace, "workspace"));
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+        return fail(KDA_ERR_INVALID, "workspace must be 256-byte aligned%s");
+    if (workspace_bytes < kda_prologue_prefill_workspace_size(dims, T, segment_tokens))
+        return fail(KDA_ERR_INVALID, "workspace too small (see kda_prologue_prefill_workspace_size)%s");
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t sbytes = (size_t)dims.H * dims.d_k * dims.d_v * sizeof(float);
+    if (T == 0) {
+        cudaError_t err = cudaMemsetAsync(workspace, 0, sizeof(int32_t), s);
+        if (err == cudaSuccess && final_state != nullptr && final_state != init_state)
+            err = init_state ? cudaMemcpyAsync(final_state, init_state, sbytes, cudaMemcpyDeviceToDevice, s)
+                             : cudaMemsetAsync(final_state, 0, sbytes, s);
+        return err == cudaSuccess ? KDA_OK : cuda_fail(err, "prologue + prefill (T = 0)");
+    }
+    const kda_dtype dt = (kda_dtype)dims.qkv_dtype;
+    const bool chunk = kda::chunk_prefill_supported(dims.d_k, dt) && !force_recurrent();
+    cudaError_t err = kda::launch_prologue_prefill(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, init_state, T,
+                                                   dims.H, dims.d_k, dt, segment_tokens, out, final_state,
+                                                   workspace, chunk, s);
+    if (err != cudaSuccess) return cuda_fail(err, "prologue + prefill launch");
+    return KDA_OK;
+}
+
 size_t kda_prefill_segmented_workspace_size(kda_dims dims, int64_t T, int32_t num_segments) {
     if (check_dims(dims) != KDA_OK || T < 0 || num_segments < 1) return 0;
     return kda::segmented_workspace_size(dims.H, dims.d_k, (kda_dtype)dims.qkv_dtype, T, num_segments);

@@ -99,6 +99,13 @@ cudaError_t launch_prologue(const void *q_raw, const void *k_raw,
                             int32_t H, int32_t D, kda_dtype dt, void *q,
                             void *k, void *v, float *g, float *beta,
                             cudaStream_t stream);
+// the same over tokens [t_begin, t_end) of the T-token inputs (the conv window
+// reaches back before t_begin); outputs q, k, v, g, beta start at row t_begin
+cudaError_t launch_prologue_range(const void *q_raw, const void *k_raw, const void *v_raw,
+                                  const float *conv_w, const float *z_g, const float *z_beta,
+                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int64_t t_begin,
+                                  int64_t t_end, int32_t H, int32_t D, kda_dtype dt, void *q,
+                                  void *k, void *v, float *g, float *beta, cudaStream_t stream);
 
 cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      const void *v, const float *g,
@@ -131,6 +138,15 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
                                  void *out, float *final_state, int32_t *status,
                                  cudaStream_t stream);
+
+// prologue and prefill of one document, segment by segment, overlapped
+size_t pipeline_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int64_t segment_tokens);
+cudaError_t launch_prologue_prefill(const void *q_raw, const void *k_raw, const void *v_raw,
+                                    const float *conv_w, const float *z_g, const float *z_beta,
+                                    const float *init_state, int64_t T, int32_t H, int32_t D,
+                                    kda_dtype dt, int64_t segment_tokens, void *out,
+                                    float *final_state, void *workspace, bool use_chunk,
+                                    cudaStream_t user);
 
 // prefill of one document as independent segments joined by an exact scan
 size_t segmented_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int32_t num_segments);

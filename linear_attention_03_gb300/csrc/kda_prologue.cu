@@ -80,7 +80,9 @@ __global__ void __launch_bounds__(kThreads, 2)
 conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
                        const Tin *__restrict__ x2, const float *__restrict__ conv_w,
                        const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
+                       int64_t t_begin, int64_t t_end,
                        Tin *__restrict__ y0, Tin *__restrict__ y1, Tin *__restrict__ y2) {
+    // tokens [t_begin, t_end) of the T-token inputs; output row 0 is token t_begin
     constexpr int TPH = D / 8;                     // lanes per head
     constexpr int HPB = kThreads / TPH;            // heads per CTA
     const int which = blockIdx.z;                  // 0 = q, 1 = k, 2 = v
@@ -104,8 +106,8 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
         w[0][e] = wv.x; w[1][e] = wv.y; w[2][e] = wv.z; w[3][e] = wv.w;
     }
 
-    const int64_t t0 = (int64_t)blockIdx.x * kTileTokens;
-    const int64_t t1 = min(T, t0 + kTileTokens);
+    const int64_t t0 = t_begin + (int64_t)blockIdx.x * kTileTokens;
+    const int64_t t1 = min(t_end, t0 + kTileTokens);
     int n = cu ? find_doc(cu, N, T, t0) : 0;
     int64_t start = clamp_off(cu, n, N, T);
     int64_t next = clamp_off(cu, n + 1, N, T);
@@ -164,7 +166,7 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
 #pragma unroll
                 for (int e = 0; e < 8; ++e) s[e] *= inv;
             }
-            if (live) Elem<Tin>::store8(y + t * row_stride + ch, s);
+            if (live) Elem<Tin>::store8(y + (t - t_begin) * row_stride + ch, s);
         }
     };
     fetch(buf0, t0);
@@ -196,14 +198,15 @@ __global__ void gates_kernel(const float *__restrict__ z_g, const float *__restr
 template <typename Tin, int D>
 cudaError_t run_conv(const void *q_raw, const void *k_raw, const void *v_raw,
                      const float *conv_w, const int32_t *cu, int32_t N, int64_t T,
-                     int32_t H, void *q, void *k, void *v, cudaStream_t stream) {
+                     int64_t t_begin, int64_t t_end, int32_t H, void *q, void *k, void *v,
+                     cudaStream_t stream) {
     constexpr int HPB = kThreads / (D / 8);
-    const dim3 grid((unsigned)((T + kTileTokens - 1) / kTileTokens),
+    const dim3 grid((unsigned)((t_end - t_begin + kTileTokens - 1) / kTileTokens),
                     (unsigned)((H + HPB - 1) / HPB), 3);
     conv_swish_norm_kernel<Tin, D><<<grid, kThreads, 0, stream>>>(
         static_cast<const Tin *>(q_raw), static_cast<const Tin *>(k_raw),
-        static_cast<const Tin *>(v_raw), conv_w, cu, N, T, H, static_cast<Tin *>(q),
-        static_cast<Tin *>(k), static_cast<Tin *>(v));
+        static_cast<const Tin *>(v_raw), conv_w, cu, N, T, H, t_begin, t_end,
+        static_cast<Tin *>(q), static_cast<Tin *>(k), static_cast<Tin *>(v));
     count_launches(1);
     return cudaGetLastError();
 }
@@ -211,37 +214,36 @@ cudaError_t run_conv(const void *q_raw, const void *k_raw, const void *v_raw,
 template <typename Tin>
 cudaError_t run_conv_d(const void *q_raw, const void *k_raw, const void *v_raw,
                        const float *conv_w, const int32_t *cu, int32_t N, int64_t T,
-                       int32_t H, int32_t D, void *q, void *k, void *v,
+                       int64_t tb, int64_t te, int32_t H, int32_t D, void *q, void *k, void *v,
                        cudaStream_t stream) {
     switch (D) {
-    case 16: return run_conv<Tin, 16>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
-    case 32: return run_conv<Tin, 32>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
-    case 64: return run_conv<Tin, 64>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
-    case 128: return run_conv<Tin, 128>(q_raw, k_raw, v_raw, conv_w, cu, N, T, H, q, k, v, stream);
+    case 16: return run_conv<Tin, 16>(q_raw, k_raw, v_raw, conv_w, cu, N, T, tb, te, H, q, k, v, stream);
+    case 32: return run_conv<Tin, 32>(q_raw, k_raw, v_raw, conv_w, cu, N, T, tb, te, H, q, k, v, stream);
+    case 64: return run_conv<Tin, 64>(q_raw, k_raw, v_raw, conv_w, cu, N, T, tb, te, H, q, k, v, stream);
+    case 128: return run_conv<Tin, 128>(q_raw, k_raw, v_raw, conv_w, cu, N, T, tb, te, H, q, k, v, stream);
     default: return cudaErrorInvalidValue;
     }
 }
 
 }  // namespace
 
-cudaError_t launch_prologue(const void *q_raw, const void *k_raw,
-                            const void *v_raw, const float *conv_w,
-                            const float *z_g, const float *z_beta,
-                            const int32_t *cu_seqlens, int32_t N, int64_t T,
-                            int32_t H, int32_t D, kda_dtype dt, void *q,
-                            void *k, void *v, float *g, float *beta,
-                            cudaStream_t stream) {
+cudaError_t launch_prologue_range(const void *q_raw, const void *k_raw, const void *v_raw,
+                                  const float *conv_w, const float *z_g, const float *z_beta,
+                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int64_t t_begin,
+                                  int64_t t_end, int32_t H, int32_t D, kda_dtype dt, void *q,
+                                  void *k, void *v, float *g, float *beta, cudaStream_t stream) {
     cudaError_t err = cudaSuccess;
-    if (T > 0) {
+    const int64_t n = t_end - t_begin;
+    if (n > 0) {
         err = dt == KDA_BF16
-                  ? run_conv_d<__nv_bfloat16>(q_raw, k_raw, v_raw, conv_w, cu_seqlens,
-                                              N, T, H, D, q, k, v, stream)
-                  : run_conv_d<float>(q_raw, k_raw, v_raw, conv_w, cu_seqlens, N, T,
-                                      H, D, q, k, v, stream);
+                  ? run_conv_d<__nv_bfloat16>(q_raw, k_raw, v_raw, conv_w, cu_seqlens, N, T,
+                                              t_begin, t_end, H, D, q, k, v, stream)
+                  : run_conv_d<float>(q_raw, k_raw, v_raw, conv_w, cu_seqlens, N, T, t_begin,
+                                      t_end, H, D, q, k, v, stream);
         if (err != cudaSuccess) return err;
     }
-    const int64_t n_g4 = z_g ? T * H * D / 4 : 0;
-    const int64_t n_b = z_beta ? T * H : 0;
+    const int64_t n_g4 = z_g ? n * H * D / 4 : 0;
+    const int64_t n_b = z_beta ? n * H : 0;
     if (n_g4 + n_b > 0) {
         int dev = 0, sms = 0;
         cudaGetDevice(&dev);
@@ -250,11 +252,24 @@ cudaError_t launch_prologue(const void *q_raw, const void *k_raw,
         int64_t blocks = (most + 255) / 256;
         if (blocks > (int64_t)sms * 8) blocks = (int64_t)sms * 8;
         if (blocks < 1) blocks = 1;
-        gates_kernel<<<(unsigned)blocks, 256, 0, stream>>>(z_g, z_beta, g, beta, n_g4, n_b);
+        gates_kernel<<<(unsigned)blocks, 256, 0, stream>>>(
+            z_g ? z_g + t_begin * H * D : nullptr, z_beta ? z_beta + t_begin * H : nullptr, g, beta,
+            n_g4, n_b);
         count_launches(1);
         err = cudaGetLastError();
     }
     return err;
+}
+
+cudaError_t launch_prologue(const void *q_raw, const void *k_raw,
+                            const void *v_raw, const float *conv_w,
+                            const float *z_g, const float *z_beta,
+                            const int32_t *cu_seqlens, int32_t N, int64_t T,
+                            int32_t H, int32_t D, kda_dtype dt, void *q,
+                            void *k, void *v, float *g, float *beta,
+                            cudaStream_t stream) {
+    return launch_prologue_range(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, cu_seqlens, N, T, 0, T, H,
+                                 D, dt, q, k, v, g, beta, stream);
 }
 
 }  // namespace kda

@@ -29,7 +29,8 @@ SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
            "kda_prologue", "kda_get_device_status", "kda_last_error",
            "kda_kernel_launches", "kda_decode_step_conv", "kda_decode_verify",
            "kda_output_gate", "kda_prefill_noalloc", "kda_selftest_wait",
-           "kda_prefill_segmented_workspace_size", "kda_prefill_segmented")
+           "kda_prefill_segmented_workspace_size", "kda_prefill_segmented",
+           "kda_prologue_prefill_workspace_size", "kda_prologue_prefill")
 
 
 class kda_dims(ctypes.Structure):
@@ -46,6 +47,10 @@ lib.kda_prefill_segmented_workspace_size.argtypes = [kda_dims, _i64, _i32]
 lib.kda_prefill_segmented_workspace_size.restype = _sz
 lib.kda_prefill_segmented.argtypes = [_P, _P, _P, _P, _P, _P, _i64, kda_dims, _i32, _P, _P, _P,
                                       _sz, _P]
+lib.kda_prologue_prefill_workspace_size.argtypes = [kda_dims, _i64, _i64]
+lib.kda_prologue_prefill_workspace_size.restype = _sz
+lib.kda_prologue_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i64, kda_dims, _i64, _P, _P, _P,
+                                     _sz, _P]
 lib.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
 lib.kda_prologue.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
                              _P, _P, _P]
@@ -59,7 +64,8 @@ lib.kda_last_error.argtypes = []
 lib.kda_last_error.restype = ctypes.c_char_p
 lib.kda_kernel_launches.argtypes = []
 lib.kda_kernel_launches.restype = ctypes.c_uint64
-for _fn in (lib.kda_prefill, lib.kda_prefill_segmented, lib.kda_decode_step, lib.kda_prologue,
+for _fn in (lib.kda_prefill, lib.kda_prefill_segmented, lib.kda_prologue_prefill,
+            lib.kda_decode_step, lib.kda_prologue,
             lib.kda_get_device_status,
             lib.kda_decode_step_conv, lib.kda_decode_verify, lib.kda_output_gate):
     _fn.restype = ctypes.c_int
@@ -187,6 +193,45 @@ def kda_prefill_segmented(q, k, v, g, beta, init_state=None, num_segments=2, out
                                    _ptr(final_state), _ptr(workspace), workspace.numel(), _stream())
     if st != KDA_OK:
         raise KDAError(st, "kda_prefill_segmented")
+    return out, final_state
+
+
+def kda_prologue_prefill_workspace_size(H: int, d: int, dtype: torch.dtype, T: int,
+                                        segment_tokens: int) -> int:
+    code = KDA_BF16 if dtype == torch.bfloat16 else KDA_F32
+    return int(lib.kda_prologue_prefill_workspace_size(kda_dims(H, d, d, code), T, segment_tokens))
+
+
+def kda_prologue_prefill(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, init_state=None,
+                         segment_tokens=16384, out=None, final_state=None, workspace=None):
+    """Prologue + prefill of one document from raw projections, segment by
+    segment with the next prologue overlapping the current prefill; returns
+    (out, final_state [H, d, d])."""
+    T, H, d = q_raw.shape
+    dev = q_raw.device
+    _dev(q_raw, "q_raw")
+    _dev(k_raw, "k_raw", q_raw.dtype, q_raw.shape)
+    _dev(v_raw, "v_raw", q_raw.dtype, q_raw.shape)
+    _dev(conv_w, "conv_w", torch.float32, (3, H * d, 4))
+    _dev(z_g, "z_g", torch.float32, q_raw.shape)
+    _dev(z_beta, "z_beta", torch.float32, (T, H))
+    _dev(init_state, "init_state", torch.float32, (H, d, d))
+    if out is None:
+        out = torch.empty_like(v_raw)
+    _dev(out, "out", q_raw.dtype, q_raw.shape)
+    if final_state is None:
+        final_state = torch.empty((H, d, d), dtype=torch.float32, device=dev)
+    _dev(final_state, "final_state", torch.float32, (H, d, d))
+    dims = dims_of(q_raw)
+    ws_bytes = int(lib.kda_prologue_prefill_workspace_size(dims, T, segment_tokens))
+    if workspace is None:
+        workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    _dev(workspace, "workspace", torch.uint8)
+    st = lib.kda_prologue_prefill(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w), _ptr(z_g),
+                                  _ptr(z_beta), _ptr(init_state), T, dims, segment_tokens, _ptr(out),
+                                  _ptr(final_state), _ptr(workspace), workspace.numel(), _stream())
+    if st != KDA_OK:
+        raise KDAError(st, "kda_prologue_prefill")
     return out, final_state
 
 

@@ -104,6 +104,21 @@ def test_segmented_prefill_argument_checks(kda):
     assert call(T=-1) == kda.KDA_ERR_INVALID
 
 
+def test_prologue_prefill_argument_checks(kda):
+    p = ctypes.c_void_p(FAKE)
+    d = dims(kda)
+    ws = kda.lib.kda_prologue_prefill_workspace_size(d, 4096, 1024)
+    assert ws > 2 * 1024 * 4 * 128 * (3 * 2 + 4)          # two segment-sized buffer sets
+    assert kda.lib.kda_prologue_prefill_workspace_size(d, 4096, 0) == 0
+    call = lambda **o: kda.lib.kda_prologue_prefill(
+        p, p, p, p, o.get("zg", p), p, None, o.get("T", 4096), d, o.get("seg", 1024), p, None,
+        o.get("ws", p), o.get("wsb", ws), None)
+    assert call(seg=0) == kda.KDA_ERR_INVALID and "segment_tokens" in kda.kda_last_error()
+    assert call(zg=None) == kda.KDA_ERR_INVALID and "z_g" in kda.kda_last_error()
+    assert call(ws=ctypes.c_void_p(FAKE + 16)) == kda.KDA_ERR_INVALID
+    assert call(wsb=ws - 1) == kda.KDA_ERR_INVALID
+
+
 def test_prologue_argument_checks(kda):
     p = ctypes.c_void_p(FAKE)
     d = dims(kda)
