@@ -80,7 +80,7 @@ constexpr uint32_t GR_L = 16384;       // L, then T: fp32, stored transposed ([c
 constexpr uint32_t LST = 72;           // padded stride (floats)
 constexpr uint32_t GR_TB = 34816;      // [Tb; 0] K-major [128][128 B]
 constexpr uint32_t GR_U = 51200;       // U MN-major, 2 halves of [64][128 B]; first the
-                                       // block-inverse scratch (10 fp32 16x16 blocks)
+                                       // block-inverse scratch (11 fp32 16x16 blocks)
 // bf16 copy of the state, MN-major B: two N halves of [128 rows][128 B]
 constexpr uint32_t OFF_S = 172032;
 // per-channel vectors of the chunk
@@ -526,13 +526,14 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             //   V31 = M32 M21 - M31,  Y30 = M31 M10 - M30;
             // stage 3: T20 = T22 V20, T31 = T33 V31 and, with T32 = -T33 M32,
             //   T30 = T33 (Y30 - M32 V20) = T33 Y30 + T32 V20.
-            // One warp per output block; scratch blocks fp32, row stride 20.
+            // One warp per output block (T30's second product on warp 0, which is
+            // free in stage 3); scratch blocks fp32, row stride 20.
             constexpr int XS = 20;
             float *X = reinterpret_cast<float *>(smem + OFF_GR + GR_U);
             auto XB = [&](int i) { return X + i * 16 * XS; };
             // block (a, b) of L or T in the transposed storage: element (r, k) at [k LST + r]
             auto LB = [&](int a, int b) { return Lf + 16 * b * LST + 16 * a; };
-            enum { M10 = 0, M21, M32, M20, M31, M30, V20, V31, Y30, T32F };
+            enum { M10 = 0, M21, M32, M20, M31, M30, V20, V31, Y30, T32F, P30 };
             // Tb block (ta, tb) = sgn * acc, column-scaled by beta, in bf16:
             // rows 16 ta + g (+8), columns 16 tb + 8 nt + 2t (+1)
             auto tb_store = [&](int ta, int tb, float sgn, const float (&acc)[2][4]) {
@@ -579,7 +580,13 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 }
             }
             ut_sync();
-            if (warp >= 3) {
+            if (warp == 0) {
+                // stage 3, the second half of T30: T32 V20 -> scratch, handed to warp 5
+                float acc[2][4] = {};
+                gemm16<false, false, false>(acc, XB(T32F), XS, XB(V20), XS, lane);
+                store_c16(acc, XB(P30), XS, lane);
+                asm volatile("bar.arrive 4, 64;" ::: "memory");
+            } else if (warp >= 3) {
                 // stage 3
                 float acc[2][4] = {};
                 if (warp == 3) {
@@ -590,7 +597,11 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     tb_store(3, 1, 1.f, acc);
                 } else {
                     gemm16<false, true, false>(acc, LB(3, 3), LST, XB(Y30), XS, lane);
-                    gemm16<false, false, false>(acc, XB(T32F), XS, XB(V20), XS, lane);
+                    asm volatile("bar.sync 4, 64;" ::: "memory");
+                    float part[2][4];
+                    load_c16(part, XB(P30), XS, lane, 1.f);
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) acc[i >> 2][i & 3] += part[i >> 2][i & 3];
                     tb_store(3, 0, 1.f, acc);
                 }
             }
@@ -623,17 +634,10 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     fence_proxy_async();
                 }
                 asm volatile("bar.sync 3, 64;" ::: "memory");
-                if (tid == 192) {
-                    if (c > 0) {
-                        tma_store_2d(&maps.o, h * kD, (int32_t)(t0 - kC), sb + OFF_G);
-                        tma_store_2d(&maps.o, h * kD + 64, (int32_t)(t0 - kC), sb + OFF_G + 8192);
-                        bulk_commit();
-                        bulk_wait_read_all();
-                    }
-                    if (c + 1 < nchunks) {
-                        issue_g(t0 + kC);
-                        misc[2] = c + 1;
-                    }
+                if (tid == 192 && c > 0) {
+                    tma_store_2d(&maps.o, h * kD, (int32_t)(t0 - kC), sb + OFF_G);
+                    tma_store_2d(&maps.o, h * kD + 64, (int32_t)(t0 - kC), sb + OFF_G + 8192);
+                    bulk_commit();
                 }
             } else if (c > 0) {
                 // warps 8..15: state rows 32 sp .. 32 sp + 31, 64 columns each
@@ -719,6 +723,13 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 mma_bf16(tmem + TM_D1, ad, bd, id, 1);
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
+        }
+        // the output stores (issued during the block inverse) have read the staging
+        // tile by now: the next chunk's g tile goes there
+        if (tid == 192 && c + 1 < nchunks) {
+            bulk_wait_read_all();
+            issue_g(t0 + kC);
+            misc[2] = c + 1;
         }
         // while the tensor core works: S <- Diag(e^{G_63}) S in TMEM, so that the
         // next MMA adds Khat^T U straight into the state
