@@ -16,6 +16,8 @@
 // three-token halo per tile) and every output written once.
 //
 // Kernel 2 (gates): elementwise g = -5 sigmoid(z_g), beta = sigmoid(z_beta).
+#include <type_traits>
+
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -74,6 +76,22 @@ template <> struct Raw8<float> {
         x[4] = b.x; x[5] = b.y; x[6] = b.z; x[7] = b.w;
     }
 };
+
+// Swish s = y sigmoid(y).  For bf16 outputs it is 0.5 y (1 + tanh(y / 2))
+// on the hardware tanh (one special-function op instead of an exponential
+// and a reciprocal; its ~5e-4 error is below the bf16 rounding of s); fp32
+// outputs keep y / (1 + e^-y).
+template <typename Tin>
+__device__ __forceinline__ float swish(float y) {
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        const float hy = 0.5f * y;
+        float t;
+        asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hy));
+        return fmaf(hy, t, hy);
+    } else {
+        return __fdividef(y, 1.f + __expf(-y));
+    }
+}
 
 template <typename Tin, int D>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -153,7 +171,7 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
             for (int e = 0; e < 8; ++e) {
                 const float yv = w[0][e] * hist[0][e] + w[1][e] * hist[1][e] +
                                  w[2][e] * hist[2][e] + w[3][e] * cur[e];
-                s[e] = __fdividef(yv, 1.f + __expf(-yv));
+                s[e] = swish<Tin>(yv);
                 ss += s[e] * s[e];
                 hist[0][e] = hist[1][e];
                 hist[1][e] = hist[2][e];
