@@ -245,32 +245,45 @@ decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
     __shared__ float4 s_part[2][C::RG][C::COLG];
 
     float *S = state + (size_t)unit * D * D;
+    const size_t vec = (size_t)unit * D;
+    const int64_t HD = (int64_t)H * D;
+    // the token's small inputs first (cached window, raw projections, taps,
+    // gate logits), so that they arrive ahead of the 64 KB state behind them
+    // and the prologue runs while the state streams in
+    Tin win[3][3], xr[3];
+    float4 wt[3];
+    float zg = 0.f;
+    if (tid < D) {
+        const Tin *raws[3] = {q_raw, k_raw, v_raw};
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            wt[i] = __ldg(reinterpret_cast<const float4 *>(conv_w + ((int64_t)i * HD + (int64_t)h * D + tid) * 4));
+            const Tin *cs = conv_state + ((size_t)n * 9 + i) * HD + (size_t)h * D + tid;  // tap 0
+            win[i][0] = cs[0]; win[i][1] = cs[3 * HD]; win[i][2] = cs[6 * HD];
+            xr[i] = raws[i][vec + tid];
+        }
+        zg = z_g[vec + tid];
+    }
     float4 s[C::ROWS];
 #pragma unroll
     for (int i = 0; i < C::ROWS; ++i)
         s[i] = __ldcs(reinterpret_cast<const float4 *>(S + (size_t)(r * C::ROWS + i) * D) + c);
 
     // prologue for channel ch = tid (tid < D): conv over the cached window
-    const size_t vec = (size_t)unit * D;
-    const int64_t HD = (int64_t)H * D;
     float yq = 0.f, yk = 0.f, yv = 0.f;
     if (tid < D) {
         const int ch = tid;
         float y3[3];
-        const Tin *raws[3] = {q_raw, k_raw, v_raw};
 #pragma unroll
         for (int i = 0; i < 3; ++i) {
-            const float4 w = __ldg(reinterpret_cast<const float4 *>(
-                conv_w + ((int64_t)i * HD + (int64_t)h * D + ch) * 4));
+            const float4 w = wt[i];
             Tin *cs = conv_state + ((size_t)n * 9 + i) * HD + (size_t)h * D + ch;  // tap 0
-            const Tin h0 = cs[0], h1 = cs[3 * HD], h2 = cs[6 * HD];
-            const Tin x = raws[i][vec + ch];
-            const float yv2 = w.x * Elem<Tin>::load(&h0) + w.y * Elem<Tin>::load(&h1) +
-                              w.z * Elem<Tin>::load(&h2) + w.w * Elem<Tin>::load(&x);
+            const float yv2 = w.x * Elem<Tin>::load(&win[i][0]) + w.y * Elem<Tin>::load(&win[i][1]) +
+                              w.z * Elem<Tin>::load(&win[i][2]) + w.w * Elem<Tin>::load(&xr[i]);
             y3[i] = __fdividef(yv2, 1.f + __expf(-yv2));
-            cs[0] = h1;                      // shift the window: t-2 -> t-3, ...
-            cs[3 * HD] = h2;
-            cs[6 * HD] = x;
+            cs[0] = win[i][1];               // shift the window: t-2 -> t-3, ...
+            cs[3 * HD] = win[i][2];
+            cs[6 * HD] = xr[i];
         }
         yq = y3[0]; yk = y3[1]; yv = y3[2];
     }
@@ -281,7 +294,7 @@ decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
     const float kq = iq * ik * sums.z;
     if (tid < D) {
         const float qq = yq * iq, kk = yk * ik;
-        const float a = __expf(-5.f / (1.f + __expf(-z_g[vec + tid])));
+        const float a = __expf(-5.f / (1.f + __expf(-zg)));
         sm.alpha[tid] = a;
         sm.k[tid] = kk;
         sm.ka[tid] = a * kk;
