@@ -317,19 +317,39 @@ decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
 // K3", Chapter 14: cached KDA states are read-only, a hit works on a private
 // copy); every draft token's output is written and state_out receives the
 // state after the first accept[n] tokens (the accepted prefix).
+//
+// Two draft tokens share each pass over the state.  Both column reductions of
+// token t+1 run on the state before token t:
+//   (D_{t+1} S_t)^T x = (alpha_{t+1} alpha_t x)^T S + ((alpha_{t+1} x) . k_t) u_t
+// for x = k_{t+1} (its error term) and x = q_{t+1} (its read), so one pass over
+// S gives four column sums, two scalars fix them up once u_t is known, and one
+// pass applies S <- D_{t+1} (D_t S + k_t u_t^T) + k_{t+1} u_{t+1}^T.
+template <int D>
+struct PairSmem {
+    float ka1[D], qa1[D];     // alpha_t k_t, alpha_t q_t
+    float ka2[D], qa2[D];     // alpha_{t+1} alpha_t k_{t+1}, alpha_{t+1} alpha_t q_{t+1}
+    float al1[D], al2[D];     // alpha_t, alpha_{t+1}
+    float k1[D], k2[D], v1[D], v2[D];
+    float red[8][4];          // per-warp partial sums of the four scalars
+    float sc[4];              // k_t.q_t, k_{t+1}.q_{t+1}, (alpha_{t+1} k_{t+1}).k_t, (alpha_{t+1} q_{t+1}).k_t
+    float beta1, beta2;
+};
+
 template <typename Tin, int D>
 __global__ void __launch_bounds__(DecodeCfg<Tin, D>::THREADS)
-verify_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
-              const float *__restrict__ g, const float *__restrict__ beta,
-              const float *__restrict__ state_in, const int32_t *__restrict__ accept,
-              int32_t K, int32_t H, Tin *__restrict__ out, float *__restrict__ state_out) {
+verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
+                   const float *__restrict__ g, const float *__restrict__ beta,
+                   const float *__restrict__ state_in, const int32_t *__restrict__ accept,
+                   int32_t K, int32_t H, Tin *__restrict__ out, float *__restrict__ state_out) {
     using C = DecodeCfg<Tin, D>;
+    static_assert(C::THREADS / 32 <= 8, "per-warp partials");
     const int unit = blockIdx.x;             // sequence * H + head
     const int n = unit / H, h = unit % H;
     const int tid = threadIdx.x;
     const int c = tid % C::COLG, r = tid / C::COLG;
-    __shared__ TokenSmem<D> sm;
-    __shared__ float4 s_part[2][C::RG][C::COLG];
+    __shared__ PairSmem<D> pm;
+    __shared__ TokenSmem<D> sm;              // the last token when K is odd
+    __shared__ float4 s_part[4][C::RG][C::COLG];
 
     const float *S0 = state_in + (size_t)unit * D * D;
     float *S1 = state_out + (size_t)unit * D * D;
@@ -345,7 +365,112 @@ verify_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
         for (int i = 0; i < C::ROWS; ++i)
             __stcs(reinterpret_cast<float4 *>(S1 + (size_t)(r * C::ROWS + i) * D) + c, s[i]);
     };
-    for (int t = 0; t < K; ++t) {
+    int t = 0;
+    for (; t + 1 < K; t += 2) {
+        if (t == acc) store_state();
+        const size_t vec1 = ((size_t)(n * K + t) * H + h) * D, vec2 = vec1 + (size_t)H * D;
+        float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (tid < D) {
+            const float k1 = Elem<Tin>::load(k + vec1 + tid), q1 = Elem<Tin>::load(q + vec1 + tid);
+            const float k2 = Elem<Tin>::load(k + vec2 + tid), q2 = Elem<Tin>::load(q + vec2 + tid);
+            const float a1 = __expf(g[vec1 + tid]), a2 = __expf(g[vec2 + tid]);
+            pm.ka1[tid] = a1 * k1; pm.qa1[tid] = a1 * q1;
+            pm.ka2[tid] = a2 * a1 * k2; pm.qa2[tid] = a2 * a1 * q2;
+            pm.al1[tid] = a1; pm.al2[tid] = a2;
+            pm.k1[tid] = k1; pm.k2[tid] = k2;
+            pm.v1[tid] = Elem<Tin>::load(v + vec1 + tid);
+            pm.v2[tid] = Elem<Tin>::load(v + vec2 + tid);
+            sc = make_float4(k1 * q1, k2 * q2, a2 * k2 * k1, a2 * q2 * k1);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sc.x += __shfl_xor_sync(0xffffffffu, sc.x, o);
+            sc.y += __shfl_xor_sync(0xffffffffu, sc.y, o);
+            sc.z += __shfl_xor_sync(0xffffffffu, sc.z, o);
+            sc.w += __shfl_xor_sync(0xffffffffu, sc.w, o);
+        }
+        if ((tid & 31) == 0) {
+            pm.red[tid >> 5][0] = sc.x; pm.red[tid >> 5][1] = sc.y;
+            pm.red[tid >> 5][2] = sc.z; pm.red[tid >> 5][3] = sc.w;
+        }
+        if (tid == 0) {
+            pm.beta1 = beta[(size_t)(n * K + t) * H + h];
+            pm.beta2 = beta[(size_t)(n * K + t + 1) * H + h];
+        }
+        __syncthreads();
+        if (tid < 4) {
+            float x = 0.f;
+#pragma unroll
+            for (int w = 0; w < C::THREADS / 32; ++w) x += pm.red[w][tid];
+            pm.sc[tid] = x;
+        }
+        // the four column sums over the old state
+        float4 p[4];
+#pragma unroll
+        for (int m = 0; m < 4; ++m) p[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+        for (int i = 0; i < C::ROWS; ++i) {
+            const int row = r * C::ROWS + i;
+            const float f[4] = {pm.ka1[row], pm.qa1[row], pm.ka2[row], pm.qa2[row]};
+#pragma unroll
+            for (int m = 0; m < 4; ++m) {
+                p[m].x += f[m] * s[i].x; p[m].y += f[m] * s[i].y;
+                p[m].z += f[m] * s[i].z; p[m].w += f[m] * s[i].w;
+            }
+        }
+#pragma unroll
+        for (int m = 0; m < 4; ++m) s_part[m][r][c] = p[m];
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) {
+            p[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int j = 0; j < C::RG; ++j) {
+                const float4 x = s_part[m][j][c];
+                p[m].x += x.x; p[m].y += x.y; p[m].z += x.z; p[m].w += x.w;
+            }
+        }
+        const float kq1 = pm.sc[0], kq2 = pm.sc[1], ck = pm.sc[2], cq = pm.sc[3];
+        const float b1 = pm.beta1, b2 = pm.beta2;
+        const float a1v[4] = {p[0].x, p[0].y, p[0].z, p[0].w}, r1v[4] = {p[1].x, p[1].y, p[1].z, p[1].w};
+        const float a2v[4] = {p[2].x, p[2].y, p[2].z, p[2].w}, r2v[4] = {p[3].x, p[3].y, p[3].z, p[3].w};
+        float u1[4], u2[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const int col = 4 * c + j;
+            u1[j] = b1 * (pm.v1[col] - a1v[j]);
+            u2[j] = b2 * (pm.v2[col] - (a2v[j] + ck * u1[j]));
+        }
+        if (r == 0) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                Elem<Tin>::store(out + vec1 + 4 * c + j, r1v[j] + u1[j] * kq1);
+                Elem<Tin>::store(out + vec2 + 4 * c + j, r2v[j] + cq * u1[j] + u2[j] * kq2);
+            }
+        }
+        // the state after token t alone, when that is the accepted prefix
+        if (t + 1 == acc) {
+#pragma unroll
+            for (int i = 0; i < C::ROWS; ++i) {
+                const int row = r * C::ROWS + i;
+                const float a = pm.al1[row], ki = pm.k1[row];
+                const float4 x = make_float4(a * s[i].x + ki * u1[0], a * s[i].y + ki * u1[1],
+                                             a * s[i].z + ki * u1[2], a * s[i].w + ki * u1[3]);
+                __stcs(reinterpret_cast<float4 *>(S1 + (size_t)row * D) + c, x);
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < C::ROWS; ++i) {
+            const int row = r * C::ROWS + i;
+            const float a1 = pm.al1[row], a2 = pm.al2[row], k1 = pm.k1[row], k2 = pm.k2[row];
+            s[i].x = a2 * (a1 * s[i].x + k1 * u1[0]) + k2 * u2[0];
+            s[i].y = a2 * (a1 * s[i].y + k1 * u1[1]) + k2 * u2[1];
+            s[i].z = a2 * (a1 * s[i].z + k1 * u1[2]) + k2 * u2[2];
+            s[i].w = a2 * (a1 * s[i].w + k1 * u1[3]) + k2 * u2[3];
+        }
+        __syncthreads();   // the next pair restages the shared inputs
+    }
+    if (t < K) {           // an odd last token, one at a time
         if (t == acc) store_state();
         const size_t vec = ((size_t)(n * K + t) * H + h) * D;
         float kqp = 0.f;
@@ -366,8 +491,8 @@ verify_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *_
             sm.beta = beta[(size_t)(n * K + t) * H + h];
         }
         __syncthreads();
-        token_update<Tin, D>(s, sm, s_part, r, c, out + vec);
-        __syncthreads();   // the next token restages the shared inputs
+        float4(&part)[2][C::RG][C::COLG] = *reinterpret_cast<float4(*)[2][C::RG][C::COLG]>(&s_part[0]);
+        token_update<Tin, D>(s, sm, part, r, c, out + vec);
     }
     if (acc == K) store_state();
 }
@@ -419,7 +544,7 @@ cudaError_t run_verify(const void *q, const void *k, const void *v, const float 
                        cudaStream_t stream) {
     const unsigned units = (unsigned)N * (unsigned)H;
     if (units == 0) return cudaSuccess;
-    verify_kernel<Tin, D><<<units, DecodeCfg<Tin, D>::THREADS, 0, stream>>>(
+    verify_pair_kernel<Tin, D><<<units, DecodeCfg<Tin, D>::THREADS, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v), g,
         beta, state_in, accept, K, H, static_cast<Tin *>(out), state_out);
     count_launches(1);

@@ -76,12 +76,17 @@ def test_decode_with_warm_conv_cache_and_state(kda):
     compare(state, ref_fin, dtype, "warm conv decode state")
 
 
-@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float32)])
-def test_verify_outputs_and_rollback_state(kda, d, dtype):
+@pytest.mark.parametrize("d,dtype,K,accept", [
+    (128, torch.bfloat16, 7, [0, 3, 7, 1, 5]),
+    (64, torch.float32, 7, [0, 3, 7, 1, 5]),
+    (128, torch.float32, 6, [2, 4, 6, 0, 5]),      # even K: every draft in a pair
+    (16, torch.bfloat16, 1, [1, 0, 1, 0, 1]),      # one draft: the odd tail alone
+    (64, torch.bfloat16, 2, [1, 2, 0, 2, 1]),
+])
+def test_verify_outputs_and_rollback_state(kda, d, dtype, K, accept):
     """K drafts per sequence from a read-only state: all outputs, and the
     state after the accepted prefix (0, some, or all drafts)."""
-    N, K, H = 5, 7, 3
-    accept = [0, 3, 7, 1, 5]
+    N, H = 5, 3
     inp = synth.custom(N * K, H, d, dtype, seed=840 + d, lengths=[K] * N, init_std=0.1)
     dv = to_device(inp)
     s_in = dv["init_state"].clone()
@@ -98,7 +103,9 @@ def test_verify_outputs_and_rollback_state(kda, d, dtype):
     _, ref_fin = oracle.recurrence(sel(inp["q"]), sel(inp["k"]), sel(inp["v"]), sel(inp["g"]),
                                    sel(inp["beta"]), f(inp["init_state"]), cu)
     compare(s_out, ref_fin, dtype, f"verify rollback state d={d}")
-    assert torch.equal(s_out[0], s_in[0])                           # accept = 0
+    for n, a in enumerate(accept):
+        if a == 0:
+            assert torch.equal(s_out[n], s_in[n])                   # nothing accepted
 
 
 @pytest.mark.parametrize("d,dtype,weighted", [(128, torch.bfloat16, True),
