@@ -277,7 +277,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         issue_v(bos, buf_off(1));
         issue_g(bos);
     }
-    // beta of the next chunk, held in a register by threads 0..63
+    // beta of the first chunk, held in a register by threads 0..63
     float beta_next = 0.f;
     if (tid < kC && nchunks > 0 && tid < len) beta_next = beta[(size_t)(bos + tid) * H + h];
 
@@ -305,7 +305,12 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         const uint32_t kbuf = buf_off(c), vbuf = buf_off(c + 1);
 
         // ---------------- step 1: this chunk's q/k/g tiles and beta
-        if (tid < kC) SM_F(OFF_BETA + 4 * tid) = beta_next;
+        if (tid < kC) {
+            SM_F(OFF_BETA + 4 * tid) = beta_next;
+            // the next chunk's beta: a whole chunk ahead, so that its latency is hidden
+            if (c + 1 < nchunks)
+                beta_next = (tid < eos - (t0 + kC)) ? beta[(size_t)(t0 + kC + tid) * H + h] : 0.f;
+        }
         wait_tma(BAR_Q, c);
         wait_tma(BAR_K, c);
         wait_tma(BAR_G, c);
@@ -610,6 +615,18 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             // outputs (D1 rows 64..127) and the bf16 copy of this chunk's incoming
             // state (TMEM state, final since the previous chunk's last MMA) for this
             // chunk's W S and Q+ S; then the zero parts of [Tb; 0]
+            // the next chunk's tiles into L2 while this warp waits, so that their
+            // loads, issued late in this chunk, hit L2
+            if (tid == 224 && c + 1 < nchunks) {
+                const int32_t y1 = (int32_t)(t0 + kC);
+                tma_prefetch_2d(&maps.q, h * kD, y1);
+                tma_prefetch_2d(&maps.q, h * kD + 64, y1);
+                tma_prefetch_2d(&maps.g, h * kD, y1);
+                tma_prefetch_2d(&maps.k, h * kD, y1);
+                tma_prefetch_2d(&maps.k, h * kD + 64, y1);
+                tma_prefetch_2d(&maps.v, h * kD, y1);
+                tma_prefetch_2d(&maps.v, h * kD + 64, y1);
+            }
             diag_done_wait();
             const int w6 = warp - 6;   // 0..9
             if (w6 == 0 || w6 == 1) {
@@ -782,8 +799,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             }
             mma_commit(sb + OFF_BAR + BAR_MMA2);
         }
-        if (tid < kC && c + 1 < nchunks)
-            beta_next = (tid < eos - (t0 + kC)) ? beta[(size_t)(t0 + kC + tid) * H + h] : 0.f;
     }
 
     // the last chunk: its outputs once its last MMAs are done
