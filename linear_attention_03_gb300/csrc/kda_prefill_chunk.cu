@@ -37,8 +37,10 @@
 //               substitution, off-diagonal blocks by block recursion)
 //   the fp32 state lives in TMEM; its bf16 copy in shared memory is the B
 //   operand of the next chunk's W S / Q+ S.
-// Decay factors are 2^x of log2-scaled G on the special-function unit; the
-// operand scalings are packed bf16x2 products (the operands are bf16 anyway).
+// Decay factors are 2^x of log2-scaled G on the special-function unit.  The
+// Gram left operand, Q+ and K+ are scaled in fp32 and rounded to bf16 once; the
+// Gram right operand rows and Khat, which multiply one bf16 row by several
+// per-channel factors, are packed bf16x2 products (two roundings).
 // All waits are bounded: a lost arrival sets KDA_DEVICE_TIMEOUT and the CTA
 // leaves after draining its own outstanding copies.
 #include <cuda.h>
@@ -170,6 +172,13 @@ __device__ __forceinline__ void store_c16(const float (&acc)[2][4], float *C, in
         *reinterpret_cast<float2 *>(C + g * sc + 8 * nt + 2 * t) = make_float2(acc[nt][0], acc[nt][1]);
         *reinterpret_cast<float2 *>(C + (g + 8) * sc + 8 * nt + 2 * t) = make_float2(acc[nt][2], acc[nt][3]);
     }
+}
+
+// element-wise product of two bf16 pairs, rounded to nearest
+__device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
+    __nv_bfloat162 x = *reinterpret_cast<__nv_bfloat162 *>(&a), y = *reinterpret_cast<__nv_bfloat162 *>(&b);
+    __nv_bfloat162 z = __hmul2(x, y);
+    return *reinterpret_cast<uint32_t *>(&z);
 }
 
 // barrier 1: the six warps of the block inverse only
@@ -377,13 +386,14 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             if (warp >= 14)   // e^{G_63}, the state decay of the chunk
                 *reinterpret_cast<float2 *>(smem + OFF_VEC + VEC_DEC + 4 * ch) = make_float2(ex2(g63.x), ex2(g63.y));
             // e^{s_ap - e_a} for the Gram right operand rows of tiles ap >= a
-            float2 pv[4];
+            uint32_t pv[4];
 #pragma unroll
             for (int ap = 0; ap < 4; ++ap)
-                pv[ap] = make_float2(ex2(tile0[ap].x - ea.x), ex2(tile0[ap].y - ea.y));
+                pv[ap] = pack_bf16x2(ex2(tile0[ap].x - ea.x), ex2(tile0[ap].y - ea.y));
             const float2 gs = make_float2(ex2(sa.x), ex2(sa.y));                    // e^{s_a}
-            const float2 kh = make_float2(ex2(g63.x - ea.x), ex2(g63.y - ea.y));    // e^{G_63 - e_a}
-            float2 kE[8], qE[8], kB[8];
+            const uint32_t kh = pack_bf16x2(ex2(g63.x - ea.x), ex2(g63.y - ea.y));    // e^{G_63 - e_a}
+            float2 kE[8], qE[8];
+            uint32_t kB[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
                 const int t = tb + i;
@@ -395,7 +405,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 const float2 Eb = make_float2(ex2(ea.x - G[i].x), ex2(ea.y - G[i].y));
                 kE[i] = make_float2(k2.x * E.x, k2.y * E.y);
                 qE[i] = make_float2(q2.x * E.x, q2.y * E.y);
-                kB[i] = make_float2(k2.x * Eb.x, k2.y * Eb.y);
+                kB[i] = pack_bf16x2(k2.x * Eb.x, k2.y * Eb.y);
                 // Gram left operand rows t (k) and 64 + t (q)
                 *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_GA + hh * 16384 + rowoff(t)) =
                     pack_bf16x2(kE[i].x, kE[i].y);
@@ -406,7 +416,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 for (int ap = 0; ap < 4; ++ap) {
                     if (ap < a) continue;
                     *reinterpret_cast<uint32_t *>(smem + OFF_GR + GR_RT + hh * RT_HALF + rowoff(gram_off(ap) + t)) =
-                        pack_bf16x2(kB[i].x * pv[ap].x, kB[i].y * pv[ap].y);
+                        mul_bf16x2(kB[i], pv[ap]);
                 }
             }
             fence_proxy_async();
@@ -432,8 +442,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     pack_bf16x2(qE[i].x * gs.x, qE[i].y * gs.y);
                 *reinterpret_cast<uint32_t *>(smem + OFF_A1 + hh * 16384 + rowoff(t)) =
                     pack_bf16x2(kE[i].x * gs.x, kE[i].y * gs.y);
-                *reinterpret_cast<uint32_t *>(smem + kbuf + hh * 8192 + rowoff(t)) =
-                    pack_bf16x2(kB[i].x * kh.x, kB[i].y * kh.y);
+                *reinterpret_cast<uint32_t *>(smem + kbuf + hh * 8192 + rowoff(t)) = mul_bf16x2(kB[i], kh);
             }
         }
         fence_proxy_async();
