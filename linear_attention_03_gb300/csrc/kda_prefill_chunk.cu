@@ -458,14 +458,13 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             tmem_ld32(tlane + TM_G + gram_off(a) + 32 * ch2, G);
             if (mine) {
                 if (sp < 2) {
-                    // L stored transposed: L[t][j] at (j LST + t)
+                    // L stored transposed: L[t][j] at (j LST + t).  Unmasked: the
+                    // block inverse reads only the strictly lower part of the
+                    // diagonal blocks and the blocks below them
                     const float bt = SM_F(OFF_BETA + 4 * t);
                     float *Lt = reinterpret_cast<float *>(smem + OFF_GR + GR_L) + t;
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        const int jj = 32 * ch2 + j;
-                        Lt[jj * LST] = (jj < t) ? bt * G[j] : 0.f;
-                    }
+                    for (int j = 0; j < 32; ++j) Lt[(32 * ch2 + j) * LST] = bt * G[j];
                 } else {
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
