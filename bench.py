@@ -458,7 +458,7 @@ def bench_extras(kda, dist, args, peaks):
     res["verify"] = {"workload": "verify: 256 sequences x 4 drafts, rollback state after 2",
                      "value": round(args.steps / (total * 1e-3), 2), "unit": "verifies/s",
                      "roofline": roofline(verify_bytes(K) * N * H, statistics.mean(per),
-                                          peaks["hbm_gbs"])}
+                                          peaks["hbm_gbs"], traffic_for("verify_pair_kernel", N))}
     del q, k, v, g, b, state, s_out, o2
     # output gate on the T=4096 shape
     T = 4096
