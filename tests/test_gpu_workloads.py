@@ -64,6 +64,23 @@ def test_workload4_long_context_with_prologue(kda):
     assert out.shape == (T, 96, 128)
 
 
+def test_workload4_pipeline_as_benchmarked(kda):
+    """The long-context workload through kda_prologue_prefill with the
+    benchmark's 16,384-token segments: the segments split at chunk
+    boundaries and carry the fp32 state, so the result is bit-identical to
+    the prologue and one prefill over the whole document (checked against the
+    oracle above)."""
+    dev = synth.inputs(4, device="cuda")
+    out_p, fin_p = kda.kda_prologue_prefill(dev["q_raw"], dev["k_raw"], dev["v_raw"], dev["conv_w"],
+                                            dev["z_g"], dev["z_beta"], None, 16384)
+    q, k, v, g, b = kda.kda_prologue(dev["q_raw"], dev["k_raw"], dev["v_raw"], dev["conv_w"],
+                                     dev["z_g"], dev["z_beta"], None)
+    del dev
+    out, fin = kda.kda_prefill(q, k, v, g, b, None, None)
+    assert torch.equal(out_p, out)
+    assert torch.equal(fin_p, fin[0])
+
+
 def test_workload5_decode(kda):
     inp = synth.inputs(5)
     dv = to_device(inp)
