@@ -4,10 +4,13 @@
 // sigmoid"), and the lower-bounded decay of "From GPT-2 to Kimi K3, from
 // first principles", Chapter 5 (g = gmin * sigmoid(z), gmin = -5).
 //
-// Kernel 1 (conv_swish_norm): one pass over a raw q, k or v tensor.  Each
-// thread owns 8 consecutive channels of one head (16-byte loads for bf16) and
-// walks a tile of 256 tokens (loads double-buffered 4 tokens ahead), keeping the last three raw inputs of its
-// channels in registers as the causal window:
+// Kernel 1 (conv_swish_norm): one pass over a raw q, k or v tensor.  A CTA
+// covers 256 consecutive tokens of a group of heads whose channels are one
+// contiguous slice of each token row (2,048 elements); the slices stream
+// through a shared-memory ring by 1-D bulk copies, two halves of several
+// tokens each, so that many bytes are in flight without holding registers.
+// Each thread owns 8 consecutive channels of one head and keeps the last
+// three raw inputs of its channels in registers as the causal window:
 //     y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t     (fp32)
 // History is zero before each document start (cu_seqlens).  Then
 // s = y * sigmoid(y); for q and k the head's d channels are scaled by
@@ -19,13 +22,19 @@
 #include <type_traits>
 
 #include "kda_internal.cuh"
+#include "kda_tc.cuh"
 
 namespace kda {
 namespace {
 
 constexpr int kThreads = 256;
 constexpr int kTileTokens = 256;  // tokens per CTA
-constexpr int kBatch = 4;         // tokens per prefetched batch
+constexpr int kSliceElems = kThreads * 8;   // one token's channels of a CTA's heads
+// tokens per half of the shared-memory ring (each half is 32 KB)
+template <typename Tin> constexpr int ring_half() { return sizeof(Tin) == 2 ? 8 : 4; }
+template <typename Tin> constexpr size_t ring_bytes() {
+    return 2 * ring_half<Tin>() * kSliceElems * sizeof(Tin) + 16;   // + two mbarriers
+}
 constexpr float kL2Eps = 1e-6f;
 constexpr float kGmin = -5.0f;
 
@@ -54,6 +63,9 @@ template <> struct Raw8<__nv_bfloat16> {
     __device__ __forceinline__ void load(const __nv_bfloat16 *p) {
         u = __ldcs(reinterpret_cast<const uint4 *>(p));
     }
+    __device__ __forceinline__ void load_shared(const __nv_bfloat16 *p) {
+        u = *reinterpret_cast<const uint4 *>(p);
+    }
     __device__ __forceinline__ void zero() { u = make_uint4(0, 0, 0, 0); }
     __device__ __forceinline__ void get(float (&x)[8]) const {
         const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -69,6 +81,10 @@ template <> struct Raw8<float> {
     __device__ __forceinline__ void load(const float *p) {
         a = __ldcs(reinterpret_cast<const float4 *>(p));
         b = __ldcs(reinterpret_cast<const float4 *>(p) + 1);
+    }
+    __device__ __forceinline__ void load_shared(const float *p) {
+        a = reinterpret_cast<const float4 *>(p)[0];
+        b = reinterpret_cast<const float4 *>(p)[1];
     }
     __device__ __forceinline__ void zero() { a = b = make_float4(0.f, 0.f, 0.f, 0.f); }
     __device__ __forceinline__ void get(float (&x)[8]) const {
@@ -139,19 +155,45 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
         r.get(hist[j]);
     }
 
-    // double-buffered batches of kBatch tokens, kept packed until used; the
-    // two slots are compile-time indices so the buffers stay in registers
-    Raw8<Tin> buf0[kBatch], buf1[kBatch];
-    auto fetch = [&](Raw8<Tin>(&bufr)[kBatch], int64_t tb) {
-#pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
-            if (live && tb + b < t1) bufr[b].load(x + (tb + b) * row_stride + ch);
-            else bufr[b].zero();
-        }
+    // the ring: two halves of HB token slices; thread 0 refills a half once
+    // every thread has read it
+    constexpr int HB = ring_half<Tin>();
+    extern __shared__ __align__(128) uint8_t ring_raw[];
+    const Tin *ring = reinterpret_cast<const Tin *>(ring_raw);
+    const uint32_t ring_s = tc::smem_u32(ring_raw);
+    const uint32_t bar = ring_s + 2 * HB * kSliceElems * (uint32_t)sizeof(Tin);
+    const int h0 = blockIdx.y * HPB;
+    const uint32_t slice_bytes = (uint32_t)(min(HPB, H - h0) * D * (int)sizeof(Tin));
+    const Tin *xs = x + (int64_t)h0 * D;            // token t's slice at xs + t * row_stride
+    if (threadIdx.x == 0) {
+        tc::mbar_init(bar, 1);
+        tc::mbar_init(bar + 8, 1);
+        tc::fence_mbar_init();
+    }
+    __syncthreads();
+    auto fill = [&](int half, int64_t tb) {       // thread 0: tokens tb .. tb+HB-1 into a half
+        const int64_t cnt = min((int64_t)HB, t1 - tb);
+        if (cnt <= 0) return;
+        const uint32_t hb = bar + 8 * half;
+        tc::mbar_expect_tx(hb, (uint32_t)cnt * slice_bytes);
+        for (int b = 0; b < cnt; ++b)
+            tc::bulk_load(ring_s + (uint32_t)((half * HB + b) * kSliceElems * sizeof(Tin)),
+                          xs + (tb + b) * row_stride, slice_bytes, hb);
     };
-    auto process = [&](const Raw8<Tin>(&bufr)[kBatch], int64_t tb) {
+    if (threadIdx.x == 0) {
+        fill(0, t0);
+        fill(1, t0 + HB);
+    }
+    const int local = (threadIdx.x / TPH) * D + 8 * sub;   // this thread's channels in a slice
+    uint32_t ph0 = 0, ph1 = 0;
+    int half = 0;
+    for (int64_t tb = t0; tb < t1; tb += HB, half ^= 1) {
+        // a lost copy ends the wait after the time limit; the outputs are then
+        // wrong but nothing hangs
+        tc::mbar_wait(bar + 8 * half, half ? ph1 : ph0);
+        if (half) ph1 ^= 1; else ph0 ^= 1;
 #pragma unroll
-        for (int b = 0; b < kBatch; ++b) {
+        for (int b = 0; b < HB; ++b) {
             const int64_t t = tb + b;
             if (t >= t1) break;                     // uniform across the CTA
             while (t >= next && n < N - 1) {        // entered a new document
@@ -164,7 +206,9 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
                     for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
             }
             float cur[8];
-            bufr[b].get(cur);
+            Raw8<Tin> r;
+            r.load_shared(ring + (half * HB + b) * kSliceElems + local);
+            r.get(cur);
             float s[8];
             float ss = 0.f;
 #pragma unroll
@@ -186,14 +230,8 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
             }
             if (live) Elem<Tin>::store8(y + (t - t_begin) * row_stride + ch, s);
         }
-    };
-    fetch(buf0, t0);
-    for (int64_t tb = t0; tb < t1; tb += 2 * kBatch) {
-        if (tb + kBatch < t1) fetch(buf1, tb + kBatch);
-        process(buf0, tb);
-        if (tb + kBatch >= t1) break;
-        if (tb + 2 * kBatch < t1) fetch(buf0, tb + 2 * kBatch);
-        process(buf1, tb + kBatch);
+        __syncthreads();                            // this half is read
+        if (threadIdx.x == 0) fill(half, tb + 2 * HB);
     }
 }
 
@@ -221,7 +259,15 @@ cudaError_t run_conv(const void *q_raw, const void *k_raw, const void *v_raw,
     constexpr int HPB = kThreads / (D / 8);
     const dim3 grid((unsigned)((t_end - t_begin + kTileTokens - 1) / kTileTokens),
                     (unsigned)((H + HPB - 1) / HPB), 3);
-    conv_swish_norm_kernel<Tin, D><<<grid, kThreads, 0, stream>>>(
+    static bool attr = false;   // per instantiation
+    if (!attr) {
+        cudaError_t e = cudaFuncSetAttribute(conv_swish_norm_kernel<Tin, D>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             (int)ring_bytes<Tin>());
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    conv_swish_norm_kernel<Tin, D><<<grid, kThreads, ring_bytes<Tin>(), stream>>>(
         static_cast<const Tin *>(q_raw), static_cast<const Tin *>(k_raw),
         static_cast<const Tin *>(v_raw), conv_w, cu, N, T, H, t_begin, t_end,
         static_cast<Tin *>(q), static_cast<Tin *>(k), static_cast<Tin *>(v));
