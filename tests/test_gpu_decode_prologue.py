@@ -75,6 +75,22 @@ def test_prologue_matches_oracle(kda, d, dtype, lengths):
     assert bool(((gg > -5) & (gg < 0)).all()) or bool(((gg >= -5) & (gg <= 0)).all())
 
 
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+def test_prologue_across_tiles_and_head_groups(kda, dtype):
+    """Documents crossing the 256-token tiles (the causal window carried from
+    the previous tile's tokens, reset at each document), and 17 heads of 128
+    channels: a full group of 16 heads per CTA and a group with one head."""
+    lengths = [300, 0, 290, 3]
+    T = sum(lengths)
+    inp = synth.custom_raw(T, 17, 128, dtype, seed=760, lengths=lengths)
+    dv = to_device(inp)
+    got = kda.kda_prologue(dv["q_raw"], dv["k_raw"], dv["v_raw"], dv["conv_w"], dv["z_g"],
+                           dv["z_beta"], torch.as_tensor(inp["cu_seqlens"], dtype=torch.int32))
+    ref = _prologue_ref(inp)
+    for name, a, b in zip("qkv", got[:3], ref[:3]):
+        compare(a, b, dtype, f"prologue {name} across tiles")
+
+
 def test_prologue_without_gates(kda):
     inp = synth.custom_raw(40, 2, 128, torch.bfloat16, seed=720)
     dv = to_device(inp)
