@@ -326,10 +326,11 @@ decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
 // pass applies S <- D_{t+1} (D_t S + k_t u_t^T) + k_{t+1} u_{t+1}^T.
 template <int D>
 struct PairSmem {
-    float ka1[D], qa1[D];     // alpha_t k_t, alpha_t q_t
-    float ka2[D], qa2[D];     // alpha_{t+1} alpha_t k_{t+1}, alpha_{t+1} alpha_t q_{t+1}
-    float al1[D], al2[D];     // alpha_t, alpha_{t+1}
-    float k1[D], k2[D], v1[D], v2[D];
+    // per state row, one 16-byte read each: the four reduction weights
+    // (alpha_t k_t, alpha_t q_t, alpha_{t+1} alpha_t k_{t+1}, alpha_{t+1} alpha_t q_{t+1})
+    // and the four update factors (alpha_t, alpha_{t+1}, k_t, k_{t+1})
+    float4 red_w[D], upd[D];
+    float v1[D], v2[D];
     float red[8][4];          // per-warp partial sums of the four scalars
     float sc[4];              // k_t.q_t, k_{t+1}.q_{t+1}, (alpha_{t+1} k_{t+1}).k_t, (alpha_{t+1} q_{t+1}).k_t
     float beta1, beta2;
@@ -374,10 +375,8 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
             const float k1 = Elem<Tin>::load(k + vec1 + tid), q1 = Elem<Tin>::load(q + vec1 + tid);
             const float k2 = Elem<Tin>::load(k + vec2 + tid), q2 = Elem<Tin>::load(q + vec2 + tid);
             const float a1 = __expf(g[vec1 + tid]), a2 = __expf(g[vec2 + tid]);
-            pm.ka1[tid] = a1 * k1; pm.qa1[tid] = a1 * q1;
-            pm.ka2[tid] = a2 * a1 * k2; pm.qa2[tid] = a2 * a1 * q2;
-            pm.al1[tid] = a1; pm.al2[tid] = a2;
-            pm.k1[tid] = k1; pm.k2[tid] = k2;
+            pm.red_w[tid] = make_float4(a1 * k1, a1 * q1, a2 * a1 * k2, a2 * a1 * q2);
+            pm.upd[tid] = make_float4(a1, a2, k1, k2);
             pm.v1[tid] = Elem<Tin>::load(v + vec1 + tid);
             pm.v2[tid] = Elem<Tin>::load(v + vec2 + tid);
             sc = make_float4(k1 * q1, k2 * q2, a2 * k2 * k1, a2 * q2 * k1);
@@ -411,7 +410,8 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
 #pragma unroll
         for (int i = 0; i < C::ROWS; ++i) {
             const int row = r * C::ROWS + i;
-            const float f[4] = {pm.ka1[row], pm.qa1[row], pm.ka2[row], pm.qa2[row]};
+            const float4 fw = pm.red_w[row];
+            const float f[4] = {fw.x, fw.y, fw.z, fw.w};
 #pragma unroll
             for (int m = 0; m < 4; ++m) {
                 p[m].x += f[m] * s[i].x; p[m].y += f[m] * s[i].y;
@@ -453,7 +453,8 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
 #pragma unroll
             for (int i = 0; i < C::ROWS; ++i) {
                 const int row = r * C::ROWS + i;
-                const float a = pm.al1[row], ki = pm.k1[row];
+                const float4 up = pm.upd[row];
+                const float a = up.x, ki = up.z;
                 const float4 x = make_float4(a * s[i].x + ki * u1[0], a * s[i].y + ki * u1[1],
                                              a * s[i].z + ki * u1[2], a * s[i].w + ki * u1[3]);
                 __stcs(reinterpret_cast<float4 *>(S1 + (size_t)row * D) + c, x);
@@ -462,7 +463,8 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
 #pragma unroll
         for (int i = 0; i < C::ROWS; ++i) {
             const int row = r * C::ROWS + i;
-            const float a1 = pm.al1[row], a2 = pm.al2[row], k1 = pm.k1[row], k2 = pm.k2[row];
+            const float4 up = pm.upd[row];
+            const float a1 = up.x, a2 = up.y, k1 = up.z, k2 = up.w;
             s[i].x = a2 * (a1 * s[i].x + k1 * u1[0]) + k2 * u2[0];
             s[i].y = a2 * (a1 * s[i].y + k1 * u1[1]) + k2 * u2[1];
             s[i].z = a2 * (a1 * s[i].z + k1 * u1[2]) + k2 * u2[2];
