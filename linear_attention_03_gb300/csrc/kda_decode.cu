@@ -129,10 +129,8 @@ decode_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 
 template <int D>
 struct TokenSmem {
-    float ka[D];      // alpha_i k_i
-    float qa[D];      // alpha_i q_i
-    float alpha[D];
-    float k[D];
+    float2 kqa[D];    // (alpha_i k_i, alpha_i q_i): one 8-byte read per state row
+    float2 ak[D];     // (alpha_i, k_i)
     float v[D];
     float red[24];    // per-warp partial sums (k.q and the L2 norms)
     float kq, beta;
@@ -151,7 +149,8 @@ __device__ __forceinline__ void token_update(float4 (&s)[DecodeCfg<Tin, D>::ROWS
 #pragma unroll
     for (int i = 0; i < C::ROWS; ++i) {
         const int row = r * C::ROWS + i;
-        const float ka = sm.ka[row], qa = sm.qa[row];
+        const float2 w = sm.kqa[row];
+        const float ka = w.x, qa = w.y;
         pa.x += ka * s[i].x; pa.y += ka * s[i].y; pa.z += ka * s[i].z; pa.w += ka * s[i].w;
         pb.x += qa * s[i].x; pb.y += qa * s[i].y; pb.z += qa * s[i].z; pb.w += qa * s[i].w;
     }
@@ -178,7 +177,8 @@ __device__ __forceinline__ void token_update(float4 (&s)[DecodeCfg<Tin, D>::ROWS
 #pragma unroll
     for (int i = 0; i < C::ROWS; ++i) {
         const int row = r * C::ROWS + i;
-        const float a = sm.alpha[row], ki = sm.k[row];
+        const float2 f = sm.ak[row];
+        const float a = f.x, ki = f.y;
         s[i].x = a * s[i].x + ki * u.x; s[i].y = a * s[i].y + ki * u.y;
         s[i].z = a * s[i].z + ki * u.z; s[i].w = a * s[i].w + ki * u.w;
     }
@@ -295,10 +295,8 @@ decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
     if (tid < D) {
         const float qq = yq * iq, kk = yk * ik;
         const float a = __expf(-5.f / (1.f + __expf(-zg)));
-        sm.alpha[tid] = a;
-        sm.k[tid] = kk;
-        sm.ka[tid] = a * kk;
-        sm.qa[tid] = a * qq;
+        sm.ak[tid] = make_float2(a, kk);
+        sm.kqa[tid] = make_float2(a * kk, a * qq);
         sm.v[tid] = yv;
     }
     if (tid == 0) {
@@ -480,10 +478,8 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
             const float ki = Elem<Tin>::load(k + vec + tid);
             const float qi = Elem<Tin>::load(q + vec + tid);
             const float a = __expf(g[vec + tid]);
-            sm.alpha[tid] = a;
-            sm.k[tid] = ki;
-            sm.ka[tid] = a * ki;
-            sm.qa[tid] = a * qi;
+            sm.ak[tid] = make_float2(a, ki);
+            sm.kqa[tid] = make_float2(a * ki, a * qi);
             sm.v[tid] = Elem<Tin>::load(v + vec + tid);
             kqp = ki * qi;
         }
