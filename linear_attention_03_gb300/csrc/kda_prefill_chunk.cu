@@ -99,6 +99,8 @@ constexpr uint32_t SMEM_BYTES = SMEM_USED + 1024;   // + alignment slack
 constexpr uint32_t BAR_Q = 0, BAR_K = 8, BAR_V = 16, BAR_G = 24, BAR_MMA = 32;
 // a chunk's last two MMA groups are issued by two threads, each committing here
 constexpr uint32_t BAR_MMA2 = 40;
+// [K+; Q+] S, issued during the block inverse
+constexpr uint32_t BAR_MMA1 = 48;
 
 // TMEM columns
 constexpr uint32_t TM_D1 = 0;     // [U ; O] accumulator
@@ -218,6 +220,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
     if (tid == 0) {
         for (int i = 0; i < 5; ++i) mbar_init(sb + OFF_BAR + 8 * i, 1);
         mbar_init(sb + OFF_BAR + BAR_MMA2, 2);
+        mbar_init(sb + OFF_BAR + BAR_MMA1, 1);
         misc[1] = 0;
         for (int i = 2; i < 6; ++i) misc[i] = 0;
         fence_mbar_init();
@@ -290,7 +293,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
     float beta_next = 0.f;
     if (tid < kC && nchunks > 0 && tid < len) beta_next = beta[(size_t)(bos + tid) * H + h];
 
-    uint32_t mma_phase = 0, mma2_phase = 0;
+    uint32_t mma_phase = 0, mma2_phase = 0, mma1_phase = 0;
     // all threads wait on the MMA barrier; a timeout raises the abort flag
     auto wait_mma = [&]() {
         if (!mbar_wait(sb + OFF_BAR + BAR_MMA, mma_phase)) misc[1] = 1;
@@ -640,8 +643,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             if (w6 == 0 || w6 == 1) {
                 // warps 6 (lanes 64..95) and 7 (lanes 96..127): the previous chunk's
                 // outputs, one token row per lane, into the staging tile (the g tile
-                // is scanned), then out with two bulk tensor stores; the next g tile
-                // is loaded once the stores have read the staging tile
+                // is scanned), then out with two bulk tensor stores
                 if (c > 0) {
                     const int t = 32 * (sp - 2) + lane;
 #pragma unroll
@@ -664,22 +666,88 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                     tma_store_2d(&maps.o, h * kD + 64, (int32_t)(t0 - kC), sb + OFF_G + 8192);
                     bulk_commit();
                 }
-            } else if (c > 0) {
-                // warps 8..15: state rows 32 sp .. 32 sp + 31, 64 columns each
+            } else {
+                // warps 8..15: the incoming state (rows 32 sp .., 64 columns each):
+                // its bf16 copy for this chunk's K+ S and Q+ S, then S <- Diag(e^{G_63}) S
+                // in TMEM so that the chunk's Khat^T U accumulates into it
                 const int c64 = (w6 - 2) >> 2;          // column half
                 const int row = 32 * sp + lane;
                 const uint32_t sdst = OFF_S + c64 * 16384;
+                const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * row);
 #pragma unroll
                 for (int q2 = 0; q2 < 2; ++q2) {
                     float v32[32];
                     tmem_ld32(tlane + TM_S + 64 * c64 + 32 * q2, v32);
+                    if (c > 0) {
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            float x[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
+                            SM_U4(sdst + sw128_off(row, 4 * q2 + i)) = pack_bf16x8(x);
+                        }
+                    }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) v32[j] *= dec;
+                    tmem_st32_nowait(tlane + TM_S + 64 * c64 + 32 * q2, v32);
+                }
+                tmem_wait_st();
+                fence_proxy_async();
+            }
+            // [K+; Q+] S into D1 once the outputs have left it and the copy is in place:
+            // rows 0..63 K+ S, rows 64..127 Q+ S (to which P U is added later)
+            tc_fence_before();
+            asm volatile("bar.sync 5, 320;" ::: "memory");
+            if (tid == 192) {
+                tc_fence_after();
+                const uint32_t id = idesc_bf16(128, 128, 0, 1);
+#pragma unroll
+                for (int kk = 0; kk < 8; ++kk) {
+                    const uint64_t ad = sw128_desc(sb + OFF_A1 + (kk >> 2) * 16384 + (kk & 3) * 32, 0, 1024);
+                    const uint64_t bd = sw128_desc(sb + OFF_S + kk * 2048, 16384, 1024);
+                    mma_bf16(tmem + TM_D1, ad, bd, id, kk > 0);
+                }
+                mma_commit(sb + OFF_BAR + BAR_MMA1);
+                // the stores have read the staging tile: the next chunk's g tile goes there
+                if (c + 1 < nchunks) {
+                    bulk_wait_read_all();
+                    issue_g(t0 + kC);
+                    misc[2] = c + 1;
+                }
+            }
+            if (w6 >= 2 && sp < 2) {
+                // warps 8, 9, 12, 13 (TMEM lanes 0..63): V - K+ S into the v buffer as
+                // the B operand of U = Tb (V - K+ S), and D1 rows 0..63 cleared for it
+                if (!mbar_wait(sb + OFF_BAR + BAR_MMA1, mma1_phase)) misc[1] = 1;
+                tc_fence_after();
+                wait_tma(BAR_V, c);
+                const int c64 = (w6 - 2) >> 2;
+                const int t = 32 * sp + lane;
+#pragma unroll
+                for (int q2 = 0; q2 < 2; ++q2) {
+                    float y32[32];
+                    tmem_ld32(tlane + TM_D1 + 64 * c64 + 32 * q2, y32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
-                        float x[8];
+                        const uint32_t off = vbuf + c64 * 8192 + sw128_off(t, 4 * q2 + i);
+                        float xv[8];
+                        unpack_bf16x8(SM_U4(off), xv);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) x[e] = v32[8 * i + e];
-                        SM_U4(sdst + sw128_off(row, 4 * q2 + i)) = pack_bf16x8(x);
+                        for (int e = 0; e < 8; ++e) xv[e] -= y32[8 * i + e];
+                        SM_U4(off) = pack_bf16x8(xv);
                     }
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) y32[j] = 0.f;
+                    tmem_st32_nowait(tlane + TM_D1 + 64 * c64 + 32 * q2, y32);
+                }
+                tmem_wait_st();
+                fence_proxy_async();
+            } else if (w6 == 9) {
+                // warp 15: q of the next chunk once [K+; Q+] S has read A1
+                if (!mbar_wait(sb + OFF_BAR + BAR_MMA1, mma1_phase)) misc[1] = 1;
+                if (tid == 480 && c + 1 < nchunks) {
+                    issue_q(t0 + kC);
+                    misc[5] = c + 1;
                 }
             }
             // rows 64..127, and the blocks above the diagonal (row tile a, 16-byte
@@ -696,82 +764,27 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 }
             }
         }
+        mma1_phase ^= 1;
         fence_proxy_async();
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- step 6: W = Tb K+ (TMEM cols 128..255), Ut = Tb V (D1 rows 0..63)
+        // ---------------- step 6: D1 rows 0..63 += Tb (V - K+ S) = U; rows 64..127 keep Q+ S
         if (tid == 0) {
             tc_fence_after();
-            wait_tma(BAR_V, c);
             const uint32_t id = idesc_bf16(128, 128, 0, 1);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
                 const uint64_t ad = sw128_desc(gr + GR_TB + kk * 32, 0, 1024);
-                mma_bf16(tmem + TM_G, ad, sw128_desc(sb + OFF_A1 + kk * 2048, 16384, 1024), id, kk > 0);
-                mma_bf16(tmem + TM_D1, ad, sw128_desc(sb + vbuf + kk * 2048, 8192, 1024), id, kk > 0);
+                mma_bf16(tmem + TM_D1, ad, sw128_desc(sb + vbuf + kk * 2048, 8192, 1024), id, 1);
             }
             mma_commit(sb + OFF_BAR + BAR_MMA);
         }
         wait_mma();
-        // v is consumed: the next chunk's k goes into its buffer (warp 14 has no
-        // part in the -W read below)
+        // v is consumed: the next chunk's k goes into its buffer
         if (tid == 448 && c + 1 < nchunks) {
             issue_k(t0 + kC, vbuf);
             misc[4] = c + 1;
-        }
-        // -W -> rows 0..63 of A1 (warps of sub-partitions 0 and 1)
-        if (sp < 2) {
-            const int t = 32 * sp + lane;
-            float v32[32];
-            tmem_ld32(tlane + TM_G + 32 * qq, v32);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                float x[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) x[e] = -v32[8 * i + e];
-                SM_U4(OFF_A1 + (qq >> 1) * 16384 + sw128_off(t, 4 * (qq & 1) + i)) = pack_bf16x8(x);
-            }
-        }
-        fence_proxy_async();
-        tc_fence_before();
-        __syncthreads();
-
-        // ---------------- step 7: D1 += [-W; Q+] S  ->  [U ; Q+ S]
-        if (tid == 0) {
-            tc_fence_after();
-            const uint32_t id = idesc_bf16(128, 128, 0, 1);
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk) {
-                const uint64_t ad = sw128_desc(sb + OFF_A1 + (kk >> 2) * 16384 + (kk & 3) * 32, 0, 1024);
-                const uint64_t bd = sw128_desc(sb + OFF_S + kk * 2048, 16384, 1024);
-                mma_bf16(tmem + TM_D1, ad, bd, id, 1);
-            }
-            mma_commit(sb + OFF_BAR + BAR_MMA);
-        }
-        // the output stores (issued during the block inverse) have read the staging
-        // tile by now: the next chunk's g tile goes there
-        if (tid == 192 && c + 1 < nchunks) {
-            bulk_wait_read_all();
-            issue_g(t0 + kC);
-            misc[2] = c + 1;
-        }
-        // while the tensor core works: S <- Diag(e^{G_63}) S in TMEM, so that the
-        // next MMA adds Khat^T U straight into the state
-        {
-            const float dec = SM_F(OFF_VEC + VEC_DEC + 4 * srow);
-            float v32[32];
-            tmem_ld32(tlane + TM_S + 32 * qq, v32);
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v32[j] *= dec;
-            tmem_st32(tlane + TM_S + 32 * qq, v32);
-        }
-        wait_mma();
-        // q of this chunk is consumed: load the next chunk's (warp 15 has no part
-        // in the U read below)
-        if (tid == 480 && c + 1 < nchunks) {
-            issue_q(t0 + kC);
-            misc[5] = c + 1;
         }
 
         // ---------------- step 8: U (D1 rows 0..63) -> bf16 MN-major B operand
@@ -836,6 +849,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             flag_status(status, KDA_DEVICE_TIMEOUT);
             mbar_wait(sb + OFF_BAR + BAR_MMA, mma_phase, 100000000ull);
             mbar_wait(sb + OFF_BAR + BAR_MMA2, mma2_phase, 100000000ull);
+            mbar_wait(sb + OFF_BAR + BAR_MMA1, mma1_phase, 100000000ull);
             const int issued[4] = {(int)misc[5], (int)misc[4], (int)misc[3], (int)misc[2]};
             const uint32_t bars[4] = {BAR_Q, BAR_K, BAR_V, BAR_G};
             for (int i = 0; i < 4; ++i)
