@@ -10,10 +10,10 @@
 //
 //   L  = strict_lower(diag(b) [k_t . k_j e^{G_t - G_j}])    (64 x 64)
 //   P  = lower_with_diag([q_t . k_j e^{G_t - G_j}])         (64 x 64)
-//   T  = (I + L)^-1,  Tb = T diag(b)
-//   W  = Tb (e^{G} * K),  Ut = Tb V                          (UT transform)
-//   U  = Ut - W S                                            (pseudo-values)
-//   O  = (e^{G} * Q) S + P U                                 (read after update)
+//   T  = (I + L)^-1,  Tb = T diag(b)                         (UT transform)
+//   U  = Tb (V - K+ S),  K+ = e^{G} * K                      (pseudo-values; the
+//        pages' W = Tb K+ and Ut = Tb V, with U = Ut - W S, re-associated)
+//   O  = Q+ S + P U,  Q+ = e^{G} * Q                         (read after update)
 //   S' = Diag(e^{G_63}) S + Khat^T U,  Khat_j = e^{G_63 - G_j} k_j
 //
 // Rescaling ("From GPT-2 to Kimi K3", Chapter 5, K3's lower-bounded decay):
@@ -36,7 +36,9 @@
 //   CUDA cores: UT solve in fp32 (16x16 diagonal blocks by forward
 //               substitution, off-diagonal blocks by block recursion)
 //   the fp32 state lives in TMEM; its bf16 copy in shared memory is the B
-//   operand of the next chunk's W S / Q+ S.
+//   operand of the chunk's [K+; Q+] S, which runs alongside the block inverse,
+//   so that after it only U = Tb (V - K+ S), the read of U and the chunk's last
+//   MMAs (O += P U, S += Khat^T U) remain.
 // Decay factors are 2^x of log2-scaled G on the special-function unit.  The
 // Gram left operand, Q+ and K+ are scaled in fp32 and rounded to bf16 once; the
 // Gram right operand rows and Khat, which multiply one bf16 row by several
@@ -59,13 +61,13 @@ constexpr int kThreads = 512;  // 16 warps: 4 per TMEM sub-partition
 constexpr float kLog2e = 1.4426950408889634f;
 
 // ---- shared memory map (bytes from a 1024-aligned base) ----
-// A1: [-W ; Q+] K-major, two K halves of [128 rows][128 B].  The q tile of a
-//     chunk is loaded by TMA into rows 64..127 and scaled in place; rows
-//     0..63 hold K+ (MN-major, channel halves 16 KB apart) until W replaces it.
+// A1: [K+ ; Q+] K-major, two K halves of [128 rows][128 B]: the A operand of
+//     [K+; Q+] S.  The q tile of a chunk is loaded by TMA into rows 64..127 and
+//     scaled in place; rows 0..63 receive K+.
 constexpr uint32_t OFF_A1 = 0;
 // two tile buffers that alternate roles: chunk c loads k into BUF[c & 1]
 // (turned into Khat in place, the MN-major A operand of Khat^T U) and v into
-// BUF[(c + 1) & 1] (the MN-major B operand of Ut = Tb V as loaded)
+// BUF[(c + 1) & 1] (overwritten by V - K+ S, the MN-major B operand of U = Tb (V - K+ S))
 constexpr uint32_t OFF_BUF0 = 32768;
 constexpr uint32_t OFF_BUF1 = 49152;
 // g tile fp32 [64][128] (TMA, no swizzle); once scanned, the staging tile of the
@@ -103,8 +105,8 @@ constexpr uint32_t BAR_MMA2 = 40;
 constexpr uint32_t BAR_MMA1 = 48;
 
 // TMEM columns
-constexpr uint32_t TM_D1 = 0;     // [U ; O] accumulator
-constexpr uint32_t TM_G = 128;    // Gram blocks (160 columns), then W
+constexpr uint32_t TM_D1 = 0;     // [K+ S ; Q+ S], then [U ; O]
+constexpr uint32_t TM_G = 128;    // Gram blocks (160 columns)
 constexpr uint32_t TM_S = 288;    // fp32 state, 128 columns; Khat^T U accumulates into it
 constexpr uint32_t TM_COLS = 512;
 
@@ -185,9 +187,6 @@ __device__ __forceinline__ uint32_t mul_bf16x2(uint32_t a, uint32_t b) {
 
 // barrier 1: the six warps of the block inverse only
 __device__ __forceinline__ void ut_sync() { asm volatile("bar.sync 1, 192;" ::: "memory"); }
-// barrier 2: the two diagonal-block warps release the ten other warps (64 + 320)
-__device__ __forceinline__ void diag_done_arrive() { asm volatile("bar.arrive 2, 384;" ::: "memory"); }
-__device__ __forceinline__ void diag_done_wait() { asm volatile("bar.sync 2, 384;" ::: "memory"); }
 
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
@@ -529,9 +528,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 for (int i = 0; i < 16; ++i)
                     SM_H(OFF_GR + GR_TB + sw128_off(16 * a5 + i, j >> 3) + (j & 7) * 2) =
                         __float2bfloat16_rn(x[i] * bj);
-                // the forward substitution waits on shared-memory latency step after
-                // step: the other warps start their traffic only once it is done
-                diag_done_arrive();
+
             }
             ut_sync();
             // 5b: off-diagonal blocks.  With D = blockdiag(T_aa) and N the
@@ -622,12 +619,11 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 }
             }
         } else {
-            // warps 6..15, once the diagonal blocks are done: the previous chunk's
-            // outputs (D1 rows 64..127) and the bf16 copy of this chunk's incoming
-            // state (TMEM state, final since the previous chunk's last MMA) for this
-            // chunk's W S and Q+ S; then the zero parts of [Tb; 0]
-            // the next chunk's tiles into L2 while this warp waits, so that their
-            // loads, issued late in this chunk, hit L2
+            // warps 6..15, alongside the block inverse: the previous chunk's outputs
+            // out of D1, the incoming state's bf16 copy and pre-scale, [K+; Q+] S
+            // into D1 and V - K+ S; then the zero parts of [Tb; 0].  First the next
+            // chunk's tiles into L2, so that their loads, issued late in this chunk,
+            // hit L2
             if (tid == 224 && c + 1 < nchunks) {
                 const int32_t y1 = (int32_t)(t0 + kC);
                 tma_prefetch_2d(&maps.q, h * kD, y1);
@@ -638,7 +634,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
                 tma_prefetch_2d(&maps.v, h * kD, y1);
                 tma_prefetch_2d(&maps.v, h * kD + 64, y1);
             }
-            diag_done_wait();
             const int w6 = warp - 6;   // 0..9
             if (w6 == 0 || w6 == 1) {
                 // warps 6 (lanes 64..95) and 7 (lanes 96..127): the previous chunk's
@@ -787,7 +782,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
             misc[4] = c + 1;
         }
 
-        // ---------------- step 8: U (D1 rows 0..63) -> bf16 MN-major B operand
+        // ---------------- step 7: U (D1 rows 0..63) -> bf16 MN-major B operand
         if (sp < 2) {
             const int t = 32 * sp + lane;
             float v32[32];
@@ -804,7 +799,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
         tc_fence_before();
         __syncthreads();
 
-        // ---------------- step 9: O = Q+ S + P U (D1 rows 64..127), S += Khat^T U.
+        // ---------------- step 8: O = Q+ S + P U (D1 rows 64..127), S += Khat^T U.
         // Not waited for here: the next chunk's loads and scan run meanwhile.
         // Two issuing threads (warps 0 and 1), one per accumulator.
         if (tid == 0 || tid == 32) {
