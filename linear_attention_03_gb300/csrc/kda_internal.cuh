@@ -5,6 +5,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "kda.h"
 
 namespace kda {
@@ -80,6 +82,21 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t code) {
 
 // Count of kernels queued by this library (kda_kernel_launches).
 void count_launches(uint64_t n);
+
+// Dynamic shared memory above the 48 KB default for `kernel`, set once per
+// device: the attribute belongs to the current device's copy of the kernel.
+// `done` is the call site's own set of devices already done (bit = device).
+template <typename Kernel>
+cudaError_t allow_dynamic_smem(Kernel *kernel, size_t bytes, std::atomic<uint64_t> &done) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev >= 0 && dev < 64 ? (uint64_t{1} << dev) : 0;
+    if (bit != 0 && (done.load(std::memory_order_relaxed) & bit) != 0) return cudaSuccess;
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+    if (e == cudaSuccess && bit != 0) done.fetch_or(bit, std::memory_order_relaxed);
+    return e;
+}
 
 // Record the thread's last-error text for kda_last_error().
 void set_last_error(kda_status code, const char *msg);

@@ -923,13 +923,9 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
         !make_map(&maps.v, v, T, H, false) || !make_map(&maps.g, g, T, H, true) ||
         !make_map(&maps.o, out, T, H, false))
         return cudaErrorInvalidValue;
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(chunk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)SMEM_BYTES);
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};
+    cudaError_t e = allow_dynamic_smem(chunk_kernel, SMEM_BYTES, smem_set);
+    if (e != cudaSuccess) return e;
     chunk_kernel<<<dim3(H, N), kThreads, SMEM_BYTES, stream>>>(
         maps, beta, init_state, cu_seqlens, N, T, H, static_cast<__nv_bfloat16 *>(out),
         final_state, status);

@@ -259,14 +259,9 @@ cudaError_t run_conv(const void *q_raw, const void *k_raw, const void *v_raw,
     constexpr int HPB = kThreads / (D / 8);
     const dim3 grid((unsigned)((t_end - t_begin + kTileTokens - 1) / kTileTokens),
                     (unsigned)((H + HPB - 1) / HPB), 3);
-    static bool attr = false;   // per instantiation
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(conv_swish_norm_kernel<Tin, D>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             (int)ring_bytes<Tin>());
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    static std::atomic<uint64_t> smem_set{0};   // per instantiation
+    cudaError_t e = allow_dynamic_smem(conv_swish_norm_kernel<Tin, D>, ring_bytes<Tin>(), smem_set);
+    if (e != cudaSuccess) return e;
     conv_swish_norm_kernel<Tin, D><<<grid, kThreads, ring_bytes<Tin>(), stream>>>(
         static_cast<const Tin *>(q_raw), static_cast<const Tin *>(k_raw),
         static_cast<const Tin *>(v_raw), conv_w, cu, N, T, H, t_begin, t_end,

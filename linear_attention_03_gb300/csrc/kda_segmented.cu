@@ -200,13 +200,8 @@ cudaError_t launch_prefill_segmented(const void *q, const void *k, const void *v
     case 32: seg_scan_kernel<32><<<H, 256, scan_smem, s>>>(R, P, Sin, final_state, n, H); break;
     case 64: seg_scan_kernel<64><<<H, 256, scan_smem, s>>>(R, P, Sin, final_state, n, H); break;
     case 128: {
-        static bool attr = false;
-        if (!attr) {
-            if ((e = cudaFuncSetAttribute(seg_scan_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                          static_cast<int>(scan_smem))) != cudaSuccess)
-                return e;
-            attr = true;
-        }
+        static std::atomic<uint64_t> smem_set{0};
+        if ((e = allow_dynamic_smem(seg_scan_kernel<128>, scan_smem, smem_set)) != cudaSuccess) return e;
         seg_scan_kernel<128><<<H, 256, scan_smem, s>>>(R, P, Sin, final_state, n, H);
         break;
     }
