@@ -349,6 +349,8 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
     __shared__ PairSmem<D> pm;
     __shared__ TokenSmem<D> sm;              // the last token when K is odd
     __shared__ float4 s_part[4][C::RG][C::COLG];
+    __shared__ float4 s_sum[4][C::COLG];     // the four column sums of a pair
+    static_assert(C::RG >= 4, "row groups 0..3 finish the four sums");
 
     const float *S0 = state_in + (size_t)unit * D * D;
     float *S1 = state_out + (size_t)unit * D * D;
@@ -419,15 +421,19 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
 #pragma unroll
         for (int m = 0; m < 4; ++m) s_part[m][r][c] = p[m];
         __syncthreads();
-#pragma unroll
-        for (int m = 0; m < 4; ++m) {
-            p[m] = make_float4(0.f, 0.f, 0.f, 0.f);
+        // row group m (< 4) finishes sum m of its column group; everyone reads the four
+        if (r < 4) {
+            float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
             for (int j = 0; j < C::RG; ++j) {
-                const float4 x = s_part[m][j][c];
-                p[m].x += x.x; p[m].y += x.y; p[m].z += x.z; p[m].w += x.w;
+                const float4 x = s_part[r][j][c];
+                x4.x += x.x; x4.y += x.y; x4.z += x.z; x4.w += x.w;
             }
+            s_sum[r][c] = x4;
         }
+        __syncthreads();
+#pragma unroll
+        for (int m = 0; m < 4; ++m) p[m] = s_sum[m][c];
         const float kq1 = pm.sc[0], kq2 = pm.sc[1], ck = pm.sc[2], cq = pm.sc[3];
         const float b1 = pm.beta1, b2 = pm.beta2;
         const float a1v[4] = {p[0].x, p[0].y, p[0].z, p[0].w}, r1v[4] = {p[1].x, p[1].y, p[1].z, p[1].w};
