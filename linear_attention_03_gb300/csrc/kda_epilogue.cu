@@ -7,8 +7,13 @@
 // trained weights):
 //     y[r, c] = o[r, c] / sqrt(mean_c o[r, c]^2 + eps) * w[c] * sigmoid(z[r, c])
 // d/8 lanes per row (token, head), 8 channels per lane; HBM-bound: o and z
-// read once, y written once.
+// read once, y written once.  The bf16 kernel keeps its two 16-byte loads as
+// packed pairs and reads the weights inside the loop, so that it fits 32
+// registers and eight 256-thread blocks fill an SM: the loads in flight per SM
+// are what sets its bandwidth.
 #include "kda_internal.cuh"
+
+#include <type_traits>
 
 namespace kda {
 namespace {
@@ -51,6 +56,62 @@ output_gate_kernel(const Tin *__restrict__ o, const Tin *__restrict__ z,
     }
 }
 
+__device__ __forceinline__ float2 bf16x2_to_float2(uint32_t u) {
+    return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xffff0000u));
+}
+
+template <int D>
+__global__ void __launch_bounds__(256, 8)
+output_gate_bf16_kernel(const __nv_bfloat16 *__restrict__ o, const __nv_bfloat16 *__restrict__ z,
+                        const float *__restrict__ weight, int64_t rows, float eps,
+                        __nv_bfloat16 *__restrict__ y) {
+    constexpr int LPR = D / 8;
+    constexpr int RPW = 32 / LPR;
+    const int lane = threadIdx.x & 31;
+    const int sub = lane % LPR, slot = lane / LPR;
+    const int64_t stride = (int64_t)gridDim.x * (blockDim.x >> 5) * RPW;
+    const float4 *w4 = reinterpret_cast<const float4 *>(weight + sub * 8);
+    for (int64_t row = ((int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5)) * RPW + slot;
+         row - slot < rows; row += stride) {
+        const bool live = row < rows;
+        uint4 ro = make_uint4(0u, 0u, 0u, 0u), rz = ro;
+        if (live) {
+            ro = __ldg(reinterpret_cast<const uint4 *>(o + row * D + sub * 8));
+            rz = __ldg(reinterpret_cast<const uint4 *>(z + row * D + sub * 8));
+        }
+        const uint32_t po[4] = {ro.x, ro.y, ro.z, ro.w}, pz[4] = {rz.x, rz.y, rz.z, rz.w};
+        float ss = 0.f;
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 a = bf16x2_to_float2(po[e]);
+            ss += a.x * a.x;
+            ss += a.y * a.y;
+        }
+#pragma unroll
+        for (int off = LPR / 2; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+        const float inv = rsqrtf(ss / D + eps);
+        if (live) {
+            float4 wa = make_float4(1.f, 1.f, 1.f, 1.f), wb = wa;
+            if (weight) {
+                wa = __ldg(w4);
+                wb = __ldg(w4 + 1);
+            }
+            const float wv[8] = {wa.x, wa.y, wa.z, wa.w, wb.x, wb.y, wb.z, wb.w};
+            uint32_t packed[4];
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                const float2 a = bf16x2_to_float2(po[e]), b = bf16x2_to_float2(pz[e]);
+                const float y0 = a.x * inv * wv[2 * e] * __fdividef(1.f, 1.f + __expf(-b.x));
+                const float y1 = a.y * inv * wv[2 * e + 1] * __fdividef(1.f, 1.f + __expf(-b.y));
+                const __nv_bfloat162 pr = __floats2bfloat162_rn(y0, y1);
+                packed[e] = *reinterpret_cast<const uint32_t *>(&pr);
+            }
+            *reinterpret_cast<uint4 *>(y + row * D + sub * 8) =
+                make_uint4(packed[0], packed[1], packed[2], packed[3]);
+        }
+    }
+}
+
 template <typename Tin, int D>
 cudaError_t run(const void *o, const void *z, const float *weight, int64_t rows, float eps,
                 void *y, cudaStream_t stream) {
@@ -60,10 +121,18 @@ cudaError_t run(const void *o, const void *z, const float *weight, int64_t rows,
     cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     const int64_t rows_per_block = 8 * (32 / (D / 8));
     int64_t blocks = (rows + rows_per_block - 1) / rows_per_block;
-    if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
-    output_gate_kernel<Tin, D><<<(unsigned)blocks, 256, 0, stream>>>(
-        static_cast<const Tin *>(o), static_cast<const Tin *>(z), weight, rows, eps,
-        static_cast<Tin *>(y));
+    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
+        // four waves of eight resident blocks per SM
+        if (blocks > (int64_t)sms * 32) blocks = (int64_t)sms * 32;
+        output_gate_bf16_kernel<D><<<(unsigned)blocks, 256, 0, stream>>>(
+            static_cast<const __nv_bfloat16 *>(o), static_cast<const __nv_bfloat16 *>(z), weight,
+            rows, eps, static_cast<__nv_bfloat16 *>(y));
+    } else {
+        if (blocks > (int64_t)sms * 16) blocks = (int64_t)sms * 16;
+        output_gate_kernel<Tin, D><<<(unsigned)blocks, 256, 0, stream>>>(
+            static_cast<const Tin *>(o), static_cast<const Tin *>(z), weight, rows, eps,
+            static_cast<Tin *>(y));
+    }
     count_launches(1);
     return cudaGetLastError();
 }

@@ -274,6 +274,18 @@ def kda_prologue(q_raw, k_raw, v_raw, conv_w, z_g=None, z_beta=None, cu_seqlens=
                 None if z_g is None else torch.empty_like(z_g),
                 None if z_beta is None else torch.empty_like(z_beta))
     q, k, v, g, beta = outs
+    _dev(q, "q", q_raw.dtype, q_raw.shape)
+    _dev(k, "k", q_raw.dtype, q_raw.shape)
+    _dev(v, "v", q_raw.dtype, q_raw.shape)
+    # the gate outputs are written (and so checked) only when their logits are given
+    if z_g is not None:
+        if g is None:
+            raise ValueError("outs must hold a g buffer when z_g is given")
+        _dev(g, "g", torch.float32, q_raw.shape)
+    if z_beta is not None:
+        if beta is None:
+            raise ValueError("outs must hold a beta buffer when z_beta is given")
+        _dev(beta, "beta", torch.float32, (T, H))
     st = lib.kda_prologue(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w), _ptr(z_g),
                           _ptr(z_beta), _ptr(cu), N, T, dims_of(q_raw), _ptr(q), _ptr(k),
                           _ptr(v), _ptr(g), _ptr(beta), _stream())
@@ -326,8 +338,10 @@ def kda_decode_verify(q, k, v, g, beta, state_in, accept, K, out=None, state_out
     _dev(acc, "accept", torch.int32, (N,))
     if out is None:
         out = torch.empty_like(v)
+    _dev(out, "out", q.dtype, q.shape)
     if state_out is None:
         state_out = torch.empty_like(state_in)
+    _dev(state_out, "state_out", torch.float32, (N, H, d, d))
     st = lib.kda_decode_verify(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(state_in),
                                _ptr(acc), N, K, dims_of(q), _ptr(out), _ptr(state_out),
                                _stream())
@@ -344,6 +358,7 @@ def kda_output_gate(o, z, weight=None, eps=1e-6, out=None):
     _dev(weight, "weight", torch.float32, (d,))
     if out is None:
         out = torch.empty_like(o)
+    _dev(out, "out", o.dtype, o.shape)
     st = lib.kda_output_gate(_ptr(o), _ptr(z), _ptr(weight), T, dims_of(o), float(eps),
                              _ptr(out), _stream())
     if st != KDA_OK:

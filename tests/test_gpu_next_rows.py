@@ -109,7 +109,11 @@ def test_verify_outputs_and_rollback_state(kda, d, dtype, K, accept):
 
 
 @pytest.mark.parametrize("d,dtype,weighted", [(128, torch.bfloat16, True),
+                                              (128, torch.bfloat16, False),
+                                              (64, torch.bfloat16, True),
+                                              (32, torch.bfloat16, False),
                                               (64, torch.float32, False),
+                                              (128, torch.float32, True),
                                               (16, torch.bfloat16, True)])
 def test_output_gate_matches_oracle(kda, d, dtype, weighted):
     T, H = 77, 3
@@ -124,3 +128,55 @@ def test_output_gate_matches_oracle(kda, d, dtype, weighted):
     oc = o.cuda()
     kda.kda_output_gate(oc, z.cuda(), None if w is None else w.cuda(), out=oc)
     compare(oc, ref, dtype, f"output gate in place d={d}")
+
+
+def test_output_gate_grid_stride_with_ragged_tail(kda):
+    """More rows than one pass of the capped grid covers (152 SMs x 32 blocks x
+    16 rows = 77,824), with a row count that ends mid-warp: every row written
+    once, none past the end."""
+    T, H, d = 1013, 97, 128                     # 98,261 rows
+    gen = torch.Generator().manual_seed(871)
+    o = torch.randn(T, H, d, generator=gen).to(torch.bfloat16)
+    z = (2 * torch.randn(T, H, d, generator=gen)).to(torch.bfloat16)
+    w = torch.rand(d, generator=gen) + 0.5
+    y = torch.full((T + 1, H, d), 7.0, dtype=torch.bfloat16, device="cuda")
+    kda.kda_output_gate(o.cuda(), z.cuda(), w.cuda(), out=y[:T])
+    ref = oracle.output_gate(f64(o), f64(z), f64(w))
+    compare(y[:T], ref, torch.bfloat16, "output gate, grid-stride rows")
+    assert torch.all(y[T] == 7.0)               # the row after the end is untouched
+
+
+def test_binding_rejects_wrong_output_buffers(kda):
+    """A caller-supplied output of the wrong shape or dtype is refused before
+    any launch (a kernel would otherwise write past its end)."""
+    T, H, d, K = 8, 2, 128, 4
+    c = lambda *s, dt=torch.float32: torch.zeros(*s, dtype=dt, device="cuda")
+    o, z = c(T, H, d, dt=torch.bfloat16), c(T, H, d, dt=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.kda_output_gate(o, z, out=c(T - 1, H, d, dt=torch.bfloat16))
+    with pytest.raises(TypeError):
+        kda.kda_output_gate(o, z, out=c(T, H, d))
+    q = c(2 * K, H, d, dt=torch.bfloat16)
+    g, b = c(2 * K, H, d), c(2 * K, H)
+    s_in = c(2, H, d, d)
+    acc = torch.tensor([1, 2], dtype=torch.int32, device="cuda")
+    with pytest.raises(ValueError):
+        kda.kda_decode_verify(q, q, q, g, b, s_in, acc, K, out=c(K, H, d, dt=torch.bfloat16))
+    with pytest.raises(ValueError):
+        kda.kda_decode_verify(q, q, q, g, b, s_in, acc, K, state_out=c(1, H, d, d))
+    raw = c(T, H, d, dt=torch.bfloat16)
+    w = c(3, H * d, 4)
+    zg, zb = c(T, H, d), c(T, H)
+    good = lambda: [torch.empty_like(raw) for _ in range(3)] + [c(T, H, d), c(T, H)]
+    bad_v = good()
+    bad_v[2] = c(T, H, d - 1, dt=torch.bfloat16)
+    with pytest.raises(ValueError):
+        kda.kda_prologue(raw, raw, raw, w, zg, zb, outs=tuple(bad_v))
+    no_g = good()
+    no_g[3] = None
+    with pytest.raises(ValueError):
+        kda.kda_prologue(raw, raw, raw, w, zg, zb, outs=tuple(no_g))
+    # gate outputs are not needed without their logits
+    q2, k2, v2, g2, b2 = kda.kda_prologue(raw, raw, raw, w, None, None,
+                                          outs=tuple(good()[:3]) + (None, None))
+    assert g2 is None and b2 is None
