@@ -471,7 +471,8 @@ def bench_extras(kda, dist, args, peaks):
     res["output_gate"] = {"workload": "head RMSNorm x sigmoid(gate), T=4096, H=96, d=128 bf16",
                           "value": round(T * args.steps / (total * 1e-3), 1), "unit": "tokens/s",
                           "roofline": roofline(GATE_BYTES * T * H, statistics.mean(per),
-                                               peaks["hbm_gbs"])}
+                                               peaks["hbm_gbs"],
+                                               traffic_for("output_gate_bf16_kernel", T))}
     del o, z, y
     # segmented prefill of one long document: with few heads the plain prefill
     # fills only H SMs; the segments give segments x H CTAs at 3x the arithmetic

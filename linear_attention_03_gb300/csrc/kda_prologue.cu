@@ -11,7 +11,8 @@
 // tokens each, so that many bytes are in flight without holding registers.
 // Each thread owns 8 consecutive channels of one head and keeps the last
 // three raw inputs of its channels in registers as the causal window:
-//     y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t     (fp32)
+//     y_t = w0 x_{t-3} + w1 x_{t-2} + w2 x_{t-1} + w3 x_t     (fp32, two
+// channels per instruction)
 // History is zero before each document start (cu_seqlens).  Then
 // s = y * sigmoid(y); for q and k the head's d channels are scaled by
 // 1 / sqrt(sum s^2 + 1e-6), the sum taken with shuffles among the d/8 lanes
@@ -93,19 +94,39 @@ template <> struct Raw8<float> {
     }
 };
 
-// Swish s = y sigmoid(y).  For bf16 outputs it is 0.5 y (1 + tanh(y / 2))
-// on the hardware tanh (one special-function op instead of an exponential
-// and a reciprocal; its ~5e-4 error is below the bf16 rounding of s); fp32
-// outputs keep y / (1 + e^-y).
+// Two fp32 lanes in one instruction (the paired FMA and multiply of sm_100
+// and later): a thread's 8 channels are 4 pairs, so the conv taps, the
+// Swish, the sum of squares and the scaling issue half the instructions.
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    unsigned long long d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)),
+          "l"(*reinterpret_cast<unsigned long long *>(&c)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float tanh_approx(float x) {
+    float t;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
+    return t;
+}
+
+// Swish s = y sigmoid(y) on a pair.  For bf16 outputs it is
+// 0.5 y (1 + tanh(y / 2)) on the hardware tanh (one special-function op
+// instead of an exponential and a reciprocal; its ~5e-4 error is below the
+// bf16 rounding of s); fp32 outputs keep y / (1 + e^-y).
 template <typename Tin>
-__device__ __forceinline__ float swish(float y) {
+__device__ __forceinline__ float2 swish2(float2 y) {
     if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
-        const float hy = 0.5f * y;
-        float t;
-        asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(hy));
-        return fmaf(hy, t, hy);
+        const float2 hy = mul2(make_float2(0.5f, 0.5f), y);
+        return fma2(hy, make_float2(tanh_approx(hy.x), tanh_approx(hy.y)), hy);
     } else {
-        return __fdividef(y, 1.f + __expf(-y));
+        return make_float2(__fdividef(y.x, 1.f + __expf(-y.x)), __fdividef(y.y, 1.f + __expf(-y.y)));
     }
 }
 
@@ -130,14 +151,19 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
     const int64_t row_stride = (int64_t)H * D;
     const int64_t ch = (int64_t)(live ? h : 0) * D + 8 * sub;   // first channel
 
-    // weights [3, H*D, 4]: the 4 taps of a channel are one float4
-    float w[4][8];
+    // weights [3, H*D, 4]: the 4 taps of a channel are one float4; held as
+    // tap x channel pair
+    float2 w[4][4];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const float4 wv = live ? __ldg(reinterpret_cast<const float4 *>(
-                                     conv_w + ((int64_t)which * row_stride + ch + e) * 4))
+    for (int e2 = 0; e2 < 4; ++e2) {
+        const float4 wa = live ? __ldg(reinterpret_cast<const float4 *>(
+                                     conv_w + ((int64_t)which * row_stride + ch + 2 * e2) * 4))
                                : make_float4(0.f, 0.f, 0.f, 0.f);
-        w[0][e] = wv.x; w[1][e] = wv.y; w[2][e] = wv.z; w[3][e] = wv.w;
+        const float4 wb = live ? __ldg(reinterpret_cast<const float4 *>(
+                                     conv_w + ((int64_t)which * row_stride + ch + 2 * e2 + 1) * 4))
+                               : make_float4(0.f, 0.f, 0.f, 0.f);
+        w[0][e2] = make_float2(wa.x, wb.x); w[1][e2] = make_float2(wa.y, wb.y);
+        w[2][e2] = make_float2(wa.z, wb.z); w[3][e2] = make_float2(wa.w, wb.w);
     }
 
     const int64_t t0 = t_begin + (int64_t)blockIdx.x * kTileTokens;
@@ -146,13 +172,16 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
     int64_t start = clamp_off(cu, n, N, T);
     int64_t next = clamp_off(cu, n + 1, N, T);
 
-    float hist[3][8];                              // x_{t-3}, x_{t-2}, x_{t-1}
+    float2 hist[3][4];                             // x_{t-3}, x_{t-2}, x_{t-1}
 #pragma unroll
     for (int j = 0; j < 3; ++j) {
         const int64_t tj = t0 - 3 + j;
         Raw8<Tin> r;
         if (live && tj >= start && tj >= 0) r.load(x + tj * row_stride + ch); else r.zero();
-        r.get(hist[j]);
+        float hv[8];
+        r.get(hv);
+#pragma unroll
+        for (int e2 = 0; e2 < 4; ++e2) hist[j][e2] = make_float2(hv[2 * e2], hv[2 * e2 + 1]);
     }
 
     // the ring: two halves of HB token slices; thread 0 refills a half once
@@ -203,31 +232,38 @@ conv_swish_norm_kernel(const Tin *__restrict__ x0, const Tin *__restrict__ x1,
 #pragma unroll
                 for (int j = 0; j < 3; ++j)
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) hist[j][e] = 0.f;
+                    for (int e2 = 0; e2 < 4; ++e2) hist[j][e2] = make_float2(0.f, 0.f);
             }
             float cur[8];
             Raw8<Tin> r;
             r.load_shared(ring + (half * HB + b) * kSliceElems + local);
             r.get(cur);
-            float s[8];
-            float ss = 0.f;
+            float2 s2[4];
+            float2 ss2 = make_float2(0.f, 0.f);
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                const float yv = w[0][e] * hist[0][e] + w[1][e] * hist[1][e] +
-                                 w[2][e] * hist[2][e] + w[3][e] * cur[e];
-                s[e] = swish<Tin>(yv);
-                ss += s[e] * s[e];
-                hist[0][e] = hist[1][e];
-                hist[1][e] = hist[2][e];
-                hist[2][e] = cur[e];
+            for (int e2 = 0; e2 < 4; ++e2) {
+                const float2 c2 = make_float2(cur[2 * e2], cur[2 * e2 + 1]);
+                float2 yv = mul2(w[0][e2], hist[0][e2]);
+                yv = fma2(w[1][e2], hist[1][e2], yv);
+                yv = fma2(w[2][e2], hist[2][e2], yv);
+                yv = fma2(w[3][e2], c2, yv);
+                s2[e2] = swish2<Tin>(yv);
+                ss2 = fma2(s2[e2], s2[e2], ss2);
+                hist[0][e2] = hist[1][e2];
+                hist[1][e2] = hist[2][e2];
+                hist[2][e2] = c2;
             }
             if (normalise) {
+                float ss = ss2.x + ss2.y;
 #pragma unroll
                 for (int o = TPH / 2; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
                 const float inv = rsqrtf(ss + kL2Eps);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) s[e] *= inv;
+                for (int e2 = 0; e2 < 4; ++e2) s2[e2] = mul2(s2[e2], make_float2(inv, inv));
             }
+            float s[8];
+#pragma unroll
+            for (int e2 = 0; e2 < 4; ++e2) { s[2 * e2] = s2[e2].x; s[2 * e2 + 1] = s2[e2].y; }
             if (live) Elem<Tin>::store8(y + (t - t_begin) * row_stride + ch, s);
         }
         __syncthreads();                            // this half is read
