@@ -37,7 +37,7 @@ import numpy as np
 import torch
 
 # stream ids, one per tensor kind
-Q, K, V, ZG, ZB, S0, CONV, LENS = 1, 2, 3, 4, 5, 6, 7, 8
+Q, K, V, ZG, ZB, S0, CONV, LENS, UNIT_S0 = 1, 2, 3, 4, 5, 6, 7, 8, 9
 
 GMIN = -5.0
 
@@ -244,3 +244,22 @@ def custom_raw(T, H, d, dtype=torch.bfloat16, seed=200, lengths=None, conv_std=0
                       torch.float32) for i in range(3)])
     res["conv_w"] = conv.permute(0, 2, 3, 1).reshape(3, H * d, 4).contiguous()
     return res
+
+
+def state_units(units, d, std=0.01, seed=300) -> np.ndarray:
+    """States [len(units), d, d] fp32 ~ std * N(0,1), one stream per unit id
+    (sequence * H + head): for tests that fill a large state on the device
+    and compare only sampled units, which are then written from here."""
+    return np.stack([std * _normal(seed, UNIT_S0, int(u), (d, d)) for u in units])
+
+
+def lengths_many(n_docs, seed=400, long_docs=()) -> list:
+    """Document lengths for the many-documents edge case: mostly 0-3 tokens,
+    one in ten 4-64 tokens; `long_docs` maps doc index -> forced length."""
+    rng = np.random.default_rng([seed, LENS])
+    short = rng.integers(0, 4, size=n_docs)
+    mid = rng.integers(4, 65, size=n_docs)
+    lengths = np.where(rng.random(n_docs) < 0.1, mid, short)
+    for i, n in dict(long_docs).items():
+        lengths[i] = n
+    return [int(x) for x in lengths]
