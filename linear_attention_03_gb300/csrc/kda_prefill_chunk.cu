@@ -110,6 +110,36 @@ constexpr uint32_t TM_G = 128;    // Gram blocks (160 columns)
 constexpr uint32_t TM_S = 288;    // fp32 state, 128 columns; Khat^T U accumulates into it
 constexpr uint32_t TM_COLS = 512;
 
+// ---- the map checked at compile time ----
+// 128-byte-swizzled operand tiles (MMA descriptors, TMA tiles) start on 1 KB
+constexpr bool kAligned1K(uint32_t off) { return off % 1024 == 0; }
+static_assert(kAligned1K(OFF_A1) && kAligned1K(OFF_BUF0) && kAligned1K(OFF_BUF1) &&
+              kAligned1K(OFF_G) && kAligned1K(OFF_S), "tile bases on 1 KB");
+static_assert(kAligned1K(OFF_GR + GR_GA) && kAligned1K(OFF_GR + GR_RT) && kAligned1K(RT_HALF) &&
+              kAligned1K(OFF_GR + GR_P) && kAligned1K(OFF_GR + GR_TB) && kAligned1K(OFF_GR + GR_U),
+              "Gram-region tiles on 1 KB");
+// regions in order, none running into the next
+static_assert(OFF_A1 + 2 * 16384 <= OFF_BUF0, "A1: [K+; Q+], two K halves of 128 x 128 B");
+static_assert(OFF_BUF0 + 16384 <= OFF_BUF1 && OFF_BUF1 + 16384 <= OFF_G, "k / v buffers, 64 x 256 B");
+static_assert(OFF_G + kC * kD * 4 <= OFF_GR, "g tile fp32 [64][128]");
+static_assert(2 * 8192 <= kC * kD * 4, "output staging (two 64-column bf16 halves) fits the g tile");
+static_assert(OFF_GR + GR_RT + 2 * RT_HALF <= OFF_S && RT_HALF >= 160 * 128,
+              "Gram right operand: 160 rows x 128 B per K half");
+static_assert(GR_GA + 2 * 16384 <= GR_RT, "Gram left operand [kE; qE], two K halves");
+static_assert(GR_P + 16384 <= GR_L && GR_L + kC * LST * 4 <= GR_TB && LST >= kC,
+              "P, then L / T transposed with a padded stride");
+static_assert(GR_TB + 16384 <= GR_U && OFF_GR + GR_U + 16384 <= OFF_S, "[Tb; 0], then U");
+static_assert(11 * 16 * 20 * 4 <= 16384, "block-inverse scratch (11 blocks, row stride 20) inside U");
+static_assert(OFF_S + 2 * 16384 <= OFF_VEC, "bf16 state copy, two N halves");
+static_assert(VEC_DEC + kD * 4 <= OFF_BETA - OFF_VEC && VEC_SEG + 8 * kD * 4 <= VEC_DEC,
+              "segment sums and chunk decay");
+static_assert(OFF_BETA + kC * 4 <= OFF_BAR, "beta of a chunk");
+static_assert(BAR_MMA1 + 8 <= OFF_MISC - OFF_BAR, "seven mbarriers");
+static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per CTA");
+// TMEM: D1 (128 columns), the Gram result (N = 160), the fp32 state (128)
+static_assert(TM_D1 + 128 <= TM_G && TM_G + 160 <= TM_S && TM_S + kD <= TM_COLS && TM_COLS <= 512,
+              "TMEM columns");
+
 // first row / column of row tile a inside the stacked Gram operand / result
 __device__ __forceinline__ uint32_t gram_off(int a) { return 8u * a * (a + 1); }  // 0,16,48,96
 __device__ __forceinline__ uint32_t buf_off(int i) { return (i & 1) ? OFF_BUF1 : OFF_BUF0; }
