@@ -422,7 +422,7 @@ def verify_bytes(K):
 GATE_BYTES = 3 * D * 2
 
 
-def bench_extras(kda, dist, args, peaks):
+def bench_extras(kda, synth, dist, args, peaks):
     """The rows beyond the core path, each timed on its own."""
     gen = torch.Generator(device="cuda").manual_seed(11)
     rnd = lambda *s, dt=torch.float32, sc=1.0: (sc * torch.randn(*s, generator=gen, device="cuda")).to(dt)
@@ -474,6 +474,32 @@ def bench_extras(kda, dist, args, peaks):
                                                peaks["hbm_gbs"],
                                                traffic_for("output_gate_bf16_kernel", T))}
     del o, z, y
+    # packed documents (8 of 512..8192 tokens, initial states given): CTAs
+    # dispatched longest first (the default workspace) against document order
+    # (a workspace with room for the status word only)
+    inp = synth.inputs(3, device="cuda")
+    cu = torch.as_tensor(inp["cu_seqlens"], dtype=torch.int32, device="cuda")
+    T, Nd = inp["q"].shape[0], cu.numel() - 1
+    po, pf = torch.empty_like(inp["q"]), torch.empty(Nd, H, D, D, device="cuda")
+    ws_full = torch.empty(kda.kda_prefill_workspace_size(H, D, torch.bfloat16, T, Nd),
+                          dtype=torch.uint8, device="cuda")
+    ws_min = torch.empty(256, dtype=torch.uint8, device="cuda")
+    packed = {}
+    for name, ws in (("longest_first", ws_full), ("document_order", ws_min)):
+        step = lambda ws=ws: kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                             inp["init_state"], cu, out=po, final_state=pf,
+                                             workspace=ws)
+        total, per = time_steps(dist, step, args.steps, args.warmup)
+        packed[name] = (total, per)
+    total, per = packed["longest_first"]
+    res["packed_documents"] = {
+        "workload": f"8 packed documents of 512..8192 tokens (T={T}), H=96, d=128 bf16, initial states",
+        "value": round(T * args.steps / (total * 1e-3), 1), "unit": "tokens/s",
+        "ms_per_step": round(total / args.steps, 4),
+        "document_order_ms_per_step": round(packed["document_order"][0] / args.steps, 4),
+        "roofline": roofline(BYTES_PER_TOKEN * T + 2 * Nd * STATE_BYTES, statistics.mean(per),
+                             peaks["hbm_gbs"])}
+    del inp, po, pf
     # segmented prefill of one long document: with few heads the plain prefill
     # fills only H SMs; the segments give segments x H CTAs at 3x the arithmetic
     for Hs, nseg in ((8, 16), (96, 2)):
@@ -590,7 +616,7 @@ def main():
         run = {"prefill": lambda: bench_prefill(kda, synth, dist, args, peaks),
                "decode": lambda: bench_decode(kda, synth, dist, args, peaks),
                "long": lambda: bench_long(kda, dist, args, peaks),
-               "extras": lambda: bench_extras(kda, dist, args, peaks)}[args.only]
+               "extras": lambda: bench_extras(kda, synth, dist, args, peaks)}[args.only]
         res = run()
         if dist.rank == 0:
             print(json.dumps({"only": args.only, "result": res}), flush=True)
@@ -613,7 +639,7 @@ def main():
     torch.cuda.empty_cache()
     lng = None if args.no_long else sampled(lambda: bench_long(kda, dist, args, peaks))[0]
     torch.cuda.empty_cache()
-    ext = sampled(lambda: bench_extras(kda, dist, args, peaks))[0]
+    ext = sampled(lambda: bench_extras(kda, synth, dist, args, peaks))[0]
     cb = None
     if dist.rank == 0 and not args.no_cpu_baseline:
         cb = cpu_baseline(synth, H)

@@ -84,10 +84,11 @@ typedef struct {
 } kda_dims;
 
 /*
- * Bytes of device workspace kda_prefill needs for T packed tokens in N
- * documents (never 0: it always holds the device status word).  The caller
- * allocates it, 256-byte aligned, and may reuse it across calls that do not
- * overlap on the GPU.
+ * Bytes of device workspace kda_prefill takes for T packed tokens in N
+ * documents: 256 for the device status word and, when N > 1, N int32 (rounded
+ * up to 256 bytes) for the order in which the documents get their CTAs,
+ * longest first.  The caller allocates it, 256-byte aligned, and may reuse it
+ * across calls that do not overlap on the GPU.
  */
 KDA_API size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N);
 
@@ -104,9 +105,13 @@ KDA_API size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N);
  *              document of T tokens)
  *   out      [T, H, d_v]  qkv_dtype, written for every token
  *   final_state [N, H, d_k, d_v] fp32 or NULL; may alias init_state
- *   workspace  kda_prefill_workspace_size() bytes; its status word is
- *              cleared by this call and set if the device finds cu_seqlens
- *              invalid (then out and final_state are unspecified).
+ *   workspace  kda_prefill_workspace_size() bytes (at least 256); its status
+ *              word is cleared by this call and set if the device finds
+ *              cu_seqlens invalid (then out and final_state are
+ *              unspecified).  With room for the order, a first small kernel
+ *              sorts the documents by length and the longest start first; a
+ *              256-byte workspace runs them in document order.  The results
+ *              are the same either way.
  * g is used as given; the tensor-core path relies on g >= -5 per token (the
  * bounded gate) to keep its 16-token rescaling factors inside fp32 range.
  * T = 0 is allowed (final_state = init_state).
@@ -297,8 +302,9 @@ KDA_API const char *kda_last_error(void);
  * deployment convenience, not part of KDA.
  * Same arguments and results as kda_prefill, minus the workspace: the
  * library keeps a fixed 64 KiB scratch array in device memory per GPU
- * (held until the process exits) and passes it as the workspace.  Problems
- * whose kda_prefill_workspace_size exceeds 64 KiB return KDA_ERR_INVALID.
+ * (held until the process exits) and passes it as the workspace.  Up to
+ * 16,320 documents the array also holds their longest-first order; larger
+ * batches run in document order, with the same results.
  *   status_out  device int32 or NULL; receives the device status word
  *               (KDA_DEVICE_*) of this call, in stream order.
  * The first call on each device looks the array's address up (the device

@@ -91,8 +91,8 @@ uint64_t kda_kernel_launches(void) { return g_launches.load(std::memory_order_re
 size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N) {
     (void)dims;
     (void)T;
-    (void)N;
-    return kStatusBytes;
+    // the status word, then (N > 1) the documents' dispatch order
+    return kStatusBytes + kda::doc_order_bytes(N);
 }
 
 kda_status kda_prefill(const void *q, const void *k, const void *v,
@@ -119,20 +119,30 @@ kda_status kda_prefill(const void *q, const void *k, const void *v,
     KDA_TRY(maybe(final_state, "final_state"));
     KDA_TRY(maybe(cu_seqlens, "cu_seqlens"));
     KDA_TRY(need(workspace, "workspace"));
-    if (workspace_bytes < kda_prefill_workspace_size(dims, T, N))
+    if (workspace_bytes < kStatusBytes)
         return fail(KDA_ERR_INVALID, "workspace too small (see kda_prefill_workspace_size)%s");
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     int32_t *status = static_cast<int32_t *>(workspace);
     cudaError_t err = cudaMemsetAsync(status, 0, sizeof(int32_t), s);
     if (err != cudaSuccess) return cuda_fail(err, "clearing the status word");
+    // several documents: their CTAs are dispatched longest first when the
+    // workspace has room for the order (else in document order)
+    const int32_t *order = nullptr;
+    if (N > 1 && T > 0 && workspace_bytes >= kStatusBytes + kda::doc_order_bytes(N)) {
+        int32_t *ord = reinterpret_cast<int32_t *>(static_cast<unsigned char *>(workspace) + kStatusBytes);
+        err = kda::launch_doc_order(cu_seqlens, N, T, ord, s);
+        if (err != cudaSuccess) return cuda_fail(err, "document order launch");
+        order = ord;
+    }
     const kda_dtype dt = (kda_dtype)dims.qkv_dtype;
     if (T > 0 && kda::chunk_prefill_supported(dims.d_k, dt) && !force_recurrent())
         err = kda::launch_prefill_chunk(q, k, v, g, beta, init_state, cu_seqlens, N, T, dims.H,
-                                        out, final_state, status, s);
+                                        out, final_state, status, s, order);
     else
         err = kda::launch_prefill_recurrent(q, k, v, g, beta, init_state, cu_seqlens, N, T,
-                                            dims.H, dims.d_k, dt, out, final_state, status, s);
+                                            dims.H, dims.d_k, dt, out, final_state, status, s,
+                                            order);
     if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
     return KDA_OK;
 }

@@ -131,7 +131,14 @@ cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      int64_t T, int32_t H, int32_t D,
                                      kda_dtype dt, void *out,
                                      float *final_state, int32_t *status,
-                                     cudaStream_t stream);
+                                     cudaStream_t stream, const int32_t *order = nullptr);
+
+// the documents of a packed batch, longest first (chunk count, decreasing):
+// order[i] is the document whose CTAs take grid row i.  doc_order_bytes(N) is
+// the room it takes in a prefill workspace (0 when N <= 1).
+size_t doc_order_bytes(int32_t N);
+cudaError_t launch_doc_order(const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t *order,
+                             cudaStream_t stream);
 
 cudaError_t launch_decode_conv(const void *q_raw, const void *k_raw, const void *v_raw,
                                const float *conv_w, void *conv_state, const float *z_g,
@@ -154,7 +161,7 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  const float *beta, const float *init_state,
                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
                                  void *out, float *final_state, int32_t *status,
-                                 cudaStream_t stream);
+                                 cudaStream_t stream, const int32_t *order = nullptr);
 
 // prologue and prefill of one document, segment by segment, overlapped
 size_t pipeline_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int64_t segment_tokens);

@@ -39,13 +39,8 @@ extern "C" kda_status kda_prefill_noalloc(const void *q, const void *k, const vo
                                           int32_t N, int64_t T, kda_dims dims, void *out,
                                           float *final_state, int32_t *status_out,
                                           void *stream) {
-    const size_t need = kda_prefill_workspace_size(dims, T, N);
-    if (need > kNoAllocScratchBytes) {
-        kda::set_last_error(KDA_ERR_INVALID,
-                            "kda_prefill_noalloc: this problem needs more scratch than the "
-                            "library's fixed 64 KiB; use kda_prefill with a workspace");
-        return KDA_ERR_INVALID;
-    }
+    // the scratch always holds the status word; up to 16,320 documents it
+    // also holds their dispatch order (larger batches run in document order)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess || dev < 0 || dev >= kMaxDevices) {

@@ -222,7 +222,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
              const float *init_state, const int32_t *__restrict__ cu, int32_t N, int64_t T,
              int32_t H, __nv_bfloat16 *__restrict__ out, float *final_state,
-             int32_t *__restrict__ status) {
+             int32_t *__restrict__ status, const int32_t *__restrict__ order) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived from the shared array so accesses stay in the shared window
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
@@ -230,7 +230,8 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ beta,
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int sp = warp & 3;          // TMEM sub-partition (lanes 32*sp .. 32*sp+31)
     const int qq = warp >> 2;         // which 32-column quarter this warp handles
-    const int h = blockIdx.x, n = blockIdx.y;
+    const int h = blockIdx.x;
+    const int n = order ? order[blockIdx.y] : static_cast<int>(blockIdx.y);   // longest first
     volatile uint32_t *misc = reinterpret_cast<volatile uint32_t *>(smem + OFF_MISC);
 #define SM_F(o) (*reinterpret_cast<float *>(smem + (o)))
 #define SM_F4(o) (*reinterpret_cast<float4 *>(smem + (o)))
@@ -947,7 +948,7 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  const float *beta, const float *init_state,
                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
                                  void *out, float *final_state, int32_t *status,
-                                 cudaStream_t stream) {
+                                 cudaStream_t stream, const int32_t *order) {
     Maps maps;
     if (!make_map(&maps.q, q, T, H, false) || !make_map(&maps.k, k, T, H, false) ||
         !make_map(&maps.v, v, T, H, false) || !make_map(&maps.g, g, T, H, true) ||
@@ -958,7 +959,7 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
     if (e != cudaSuccess) return e;
     chunk_kernel<<<dim3(H, N), kThreads, SMEM_BYTES, stream>>>(
         maps, beta, init_state, cu_seqlens, N, T, H, static_cast<__nv_bfloat16 *>(out),
-        final_state, status);
+        final_state, status, order);
     count_launches(1);
     return cudaGetLastError();
 }

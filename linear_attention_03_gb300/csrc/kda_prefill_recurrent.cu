@@ -28,12 +28,12 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  const float *__restrict__ beta, const float *init_state,
                  const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
                  Tin *__restrict__ out, float *final_state,
-                 int32_t *__restrict__ status) {
+                 int32_t *__restrict__ status, const int32_t *__restrict__ order) {
     constexpr int NW = (D + 31) / 32;
     constexpr int LANES = D < 32 ? D : 32;           // lanes of a (partial) warp
     constexpr unsigned MASK = D < 32 ? ((1u << D) - 1u) : 0xffffffffu;
     const int h = blockIdx.x;
-    const int n = blockIdx.y;
+    const int n = order ? order[blockIdx.y] : static_cast<int>(blockIdx.y);   // longest first
     const int j = threadIdx.x;
     int64_t bos, eos;
     if (!doc_bounds(cu, n, N, T, bos, eos)) {
@@ -113,11 +113,11 @@ template <typename Tin, int D>
 cudaError_t run(const void *q, const void *k, const void *v, const float *g,
                 const float *beta, const float *init_state, const int32_t *cu,
                 int32_t N, int64_t T, int32_t H, void *out, float *final_state,
-                int32_t *status, cudaStream_t stream) {
+                int32_t *status, cudaStream_t stream, const int32_t *order) {
     recurrent_kernel<Tin, D><<<dim3(H, N), D, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k),
         static_cast<const Tin *>(v), g, beta, init_state, cu, N, T, H,
-        static_cast<Tin *>(out), final_state, status);
+        static_cast<Tin *>(out), final_state, status, order);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -126,12 +126,12 @@ template <typename Tin>
 cudaError_t run_d(const void *q, const void *k, const void *v, const float *g,
                   const float *beta, const float *init_state, const int32_t *cu,
                   int32_t N, int64_t T, int32_t H, int32_t D, void *out,
-                  float *final_state, int32_t *status, cudaStream_t stream) {
+                  float *final_state, int32_t *status, cudaStream_t stream, const int32_t *order) {
     switch (D) {
-    case 16: return run<Tin, 16>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream);
-    case 32: return run<Tin, 32>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream);
-    case 64: return run<Tin, 64>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream);
-    case 128: return run<Tin, 128>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream);
+    case 16: return run<Tin, 16>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
+    case 32: return run<Tin, 32>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
+    case 64: return run<Tin, 64>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
+    case 128: return run<Tin, 128>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -145,12 +145,12 @@ cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      int64_t T, int32_t H, int32_t D,
                                      kda_dtype dt, void *out,
                                      float *final_state, int32_t *status,
-                                     cudaStream_t stream) {
+                                     cudaStream_t stream, const int32_t *order) {
     if (dt == KDA_BF16)
         return run_d<__nv_bfloat16>(q, k, v, g, beta, init_state, cu_seqlens, N, T, H, D,
-                                    out, final_state, status, stream);
+                                    out, final_state, status, stream, order);
     return run_d<float>(q, k, v, g, beta, init_state, cu_seqlens, N, T, H, D, out,
-                        final_state, status, stream);
+                        final_state, status, stream, order);
 }
 
 }  // namespace kda

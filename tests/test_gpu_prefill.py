@@ -110,3 +110,31 @@ def test_bounded_wait_reports_timeout(kda):
     inp = to_device(synth.custom(20, 2, 128, torch.bfloat16, seed=505))
     kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], None, None, workspace=ws)
     assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_OK
+
+
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float32)])
+def test_longest_first_dispatch_changes_no_result(kda, d, dtype):
+    """Packed documents of mixed lengths: with the default workspace the
+    documents get their CTAs longest first (the order a first kernel leaves
+    after the status word); with a 256-byte workspace they run in document
+    order.  Outputs and states are bit-identical, and the oracle agrees."""
+    lengths = [5, 300, 0, 64, 1200, 17, 65, 0, 640, 1, 129, 900]
+    N, T, H = len(lengths), sum(lengths), 3
+    inp = synth.custom(T, H, d, dtype, seed=450 + d, lengths=lengths, init_std=0.05)
+    dv = to_device(inp)
+    ws_size = kda.kda_prefill_workspace_size(H, d, dtype, T, N)
+    assert ws_size >= 256 + 4 * N
+    ws_big = torch.full((ws_size,), 0xAB, dtype=torch.uint8, device="cuda")
+    ws_small = torch.empty(256, dtype=torch.uint8, device="cuda")
+    out_a, fin_a = gpu_prefill(kda, dv, workspace=ws_big)
+    out_b, fin_b = gpu_prefill(kda, dv, workspace=ws_small)
+    assert torch.equal(out_a, out_b) and torch.equal(fin_a, fin_b)
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out_a, ref_out, dtype, f"packed out d={d}")
+    compare(fin_a, ref_fin, dtype, f"packed state d={d}")
+    # the order: a permutation of the documents, chunk counts non-increasing
+    # (every count here is below 128 chunks, where the buckets are exact)
+    order = ws_big[256:256 + 4 * N].view(torch.int32).cpu().tolist()
+    assert sorted(order) == list(range(N))
+    chunks = [-(-lengths[n] // 64) for n in order]
+    assert chunks == sorted(chunks, reverse=True)
