@@ -254,6 +254,7 @@ KDA_API kda_status kda_decode_step_conv(const void *q_raw, const void *k_raw, co
  *   q, k, g [N*K, H, d] (row n*K + t is draft t of sequence n); v, out
  *   likewise; beta [N*K, H]; state_in, state_out [N, H, d, d] fp32 (must not
  *   alias); accept [N] int32 device, clamped to 0..K.
+ * N * K * H and 2 * N * H must not exceed 2^31 - 1 (KDA_ERR_INVALID).
  */
 KDA_API kda_status kda_decode_verify(const void *q, const void *k, const void *v, const float *g,
                                      const float *beta, const float *state_in,

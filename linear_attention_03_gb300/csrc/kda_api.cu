@@ -331,6 +331,8 @@ kda_status kda_decode_verify(const void *q, const void *k, const void *v, const 
     KDA_TRY(check_dims(dims));
     if (N < 0 || K < 1) return fail(KDA_ERR_INVALID, "N must be >= 0 and K >= 1%s");
     if ((int64_t)N * K * dims.H > INT32_MAX) return fail(KDA_ERR_INVALID, "N * K * H too large%s");
+    // up to two CTAs per (sequence, head)
+    if ((int64_t)N * dims.H * 2 > INT32_MAX) return fail(KDA_ERR_INVALID, "N * H too large%s");
     if (N == 0) return KDA_OK;
     KDA_TRY(need(q, "q"));
     KDA_TRY(need(k, "k"));

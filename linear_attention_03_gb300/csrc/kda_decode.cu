@@ -321,7 +321,9 @@ decode_conv_kernel(const Tin *__restrict__ q_raw, const Tin *__restrict__ k_raw,
 //   (D_{t+1} S_t)^T x = (alpha_{t+1} alpha_t x)^T S + ((alpha_{t+1} x) . k_t) u_t
 // for x = k_{t+1} (its error term) and x = q_{t+1} (its read), so one pass over
 // S gives four column sums, two scalars fix them up once u_t is known, and one
-// pass applies S <- D_{t+1} (D_t S + k_t u_t^T) + k_{t+1} u_{t+1}^T.
+// pass applies S <- D_{t+1} (D_t S + k_t u_t^T) + k_{t+1} u_{t+1}^T.  An odd
+// last draft runs as a pair whose second token is neutral (alpha = 1,
+// k = q = v = beta = 0: u = 0 and the state passes through), with no output.
 template <int D>
 struct PairSmem {
     // per state row, one 16-byte read each: the four reduction weights
@@ -334,20 +336,38 @@ struct PairSmem {
     float beta1, beta2;
 };
 
+// The state's columns are independent here too (the column sums, the update
+// and the scalars k.q, (alpha k').k need no other column), so for d >= 64
+// verify gives each (sequence, head) SPLIT = 2 CTAs of half the columns.
+// Each thread keeps its 16 rows x 4 columns; a CTA has half the warps behind
+// each of its barriers, and four 128-thread CTAs fit an SM where two 256-thread
+// ones did, so one CTA's barrier wait is covered by three others (the top
+// stall of the one-CTA form).  Each CTA stages the token vectors whole, one
+// thread per channel.
 template <typename Tin, int D>
-__global__ void __launch_bounds__(DecodeCfg<Tin, D>::THREADS)
+struct VerifyCfg {
+    static constexpr int SPLIT = D >= 64 ? 2 : 1;
+    static constexpr int COLG = D / 4 / SPLIT;         // float4 column groups of a CTA
+    static constexpr int RG = 8;
+    static constexpr int ROWS = D / RG;
+    static constexpr int THREADS = COLG * RG;
+};
+
+template <typename Tin, int D>
+__global__ void __launch_bounds__(VerifyCfg<Tin, D>::THREADS)
 verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const Tin *__restrict__ v,
                    const float *__restrict__ g, const float *__restrict__ beta,
                    const float *__restrict__ state_in, const int32_t *__restrict__ accept,
                    int32_t K, int32_t H, Tin *__restrict__ out, float *__restrict__ state_out) {
-    using C = DecodeCfg<Tin, D>;
+    using C = VerifyCfg<Tin, D>;
     static_assert(C::THREADS / 32 <= 8, "per-warp partials");
-    const int unit = blockIdx.x;             // sequence * H + head
+    static_assert(C::THREADS >= D, "one thread per channel stages the vectors");
+    const int unit = blockIdx.x / C::SPLIT;  // sequence * H + head
+    const int col0 = (blockIdx.x % C::SPLIT) * (D / C::SPLIT);   // this CTA's first column
     const int n = unit / H, h = unit % H;
     const int tid = threadIdx.x;
     const int c = tid % C::COLG, r = tid / C::COLG;
     __shared__ PairSmem<D> pm;
-    __shared__ TokenSmem<D> sm;              // the last token when K is odd
     __shared__ float4 s_part[4][C::RG][C::COLG];
     __shared__ float4 s_sum[4][C::COLG];     // the four column sums of a pair
     static_assert(C::RG >= 4, "row groups 0..3 finish the four sums");
@@ -357,28 +377,31 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
     float4 s[C::ROWS];
 #pragma unroll
     for (int i = 0; i < C::ROWS; ++i)
-        s[i] = __ldcs(reinterpret_cast<const float4 *>(S0 + (size_t)(r * C::ROWS + i) * D) + c);
+        s[i] = __ldcs(reinterpret_cast<const float4 *>(S0 + (size_t)(r * C::ROWS + i) * D + col0) + c);
     int acc = accept[n];
     acc = acc < 0 ? 0 : (acc > K ? K : acc);
 
     auto store_state = [&]() {
 #pragma unroll
         for (int i = 0; i < C::ROWS; ++i)
-            __stcs(reinterpret_cast<float4 *>(S1 + (size_t)(r * C::ROWS + i) * D) + c, s[i]);
+            __stcs(reinterpret_cast<float4 *>(S1 + (size_t)(r * C::ROWS + i) * D + col0) + c, s[i]);
     };
-    int t = 0;
-    for (; t + 1 < K; t += 2) {
+    // one pass over the state for drafts t and t + 1; two = false: t is the
+    // last draft and the second token is neutral.  (A compile-time flag, with
+    // the pass inlined twice, took 127 registers and ran 3% slower.)
+    auto pass = [&](const int t, const bool two) {
         if (t == acc) store_state();
         const size_t vec1 = ((size_t)(n * K + t) * H + h) * D, vec2 = vec1 + (size_t)H * D;
         float4 sc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (tid < D) {
             const float k1 = Elem<Tin>::load(k + vec1 + tid), q1 = Elem<Tin>::load(q + vec1 + tid);
-            const float k2 = Elem<Tin>::load(k + vec2 + tid), q2 = Elem<Tin>::load(q + vec2 + tid);
-            const float a1 = __expf(g[vec1 + tid]), a2 = __expf(g[vec2 + tid]);
+            const float k2 = two ? Elem<Tin>::load(k + vec2 + tid) : 0.f;
+            const float q2 = two ? Elem<Tin>::load(q + vec2 + tid) : 0.f;
+            const float a1 = __expf(g[vec1 + tid]), a2 = two ? __expf(g[vec2 + tid]) : 1.f;
             pm.red_w[tid] = make_float4(a1 * k1, a1 * q1, a2 * a1 * k2, a2 * a1 * q2);
             pm.upd[tid] = make_float4(a1, a2, k1, k2);
             pm.v1[tid] = Elem<Tin>::load(v + vec1 + tid);
-            pm.v2[tid] = Elem<Tin>::load(v + vec2 + tid);
+            pm.v2[tid] = two ? Elem<Tin>::load(v + vec2 + tid) : 0.f;
             sc = make_float4(k1 * q1, k2 * q2, a2 * k2 * k1, a2 * q2 * k1);
         }
 #pragma unroll
@@ -394,7 +417,7 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
         }
         if (tid == 0) {
             pm.beta1 = beta[(size_t)(n * K + t) * H + h];
-            pm.beta2 = beta[(size_t)(n * K + t + 1) * H + h];
+            pm.beta2 = two ? beta[(size_t)(n * K + t + 1) * H + h] : 0.f;
         }
         __syncthreads();
         if (tid < 4) {
@@ -441,15 +464,16 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
         float u1[4], u2[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
-            const int col = 4 * c + j;
+            const int col = col0 + 4 * c + j;
             u1[j] = b1 * (pm.v1[col] - a1v[j]);
             u2[j] = b2 * (pm.v2[col] - (a2v[j] + ck * u1[j]));
         }
         if (r == 0) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) {
-                Elem<Tin>::store(out + vec1 + 4 * c + j, r1v[j] + u1[j] * kq1);
-                Elem<Tin>::store(out + vec2 + 4 * c + j, r2v[j] + cq * u1[j] + u2[j] * kq2);
+                Elem<Tin>::store(out + vec1 + col0 + 4 * c + j, r1v[j] + u1[j] * kq1);
+                if (two)
+                    Elem<Tin>::store(out + vec2 + col0 + 4 * c + j, r2v[j] + cq * u1[j] + u2[j] * kq2);
             }
         }
         // the state after token t alone, when that is the accepted prefix
@@ -461,7 +485,7 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
                 const float a = up.x, ki = up.z;
                 const float4 x = make_float4(a * s[i].x + ki * u1[0], a * s[i].y + ki * u1[1],
                                              a * s[i].z + ki * u1[2], a * s[i].w + ki * u1[3]);
-                __stcs(reinterpret_cast<float4 *>(S1 + (size_t)row * D) + c, x);
+                __stcs(reinterpret_cast<float4 *>(S1 + (size_t)row * D + col0) + c, x);
             }
         }
 #pragma unroll
@@ -475,30 +499,10 @@ verify_pair_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k, const T
             s[i].w = a2 * (a1 * s[i].w + k1 * u1[3]) + k2 * u2[3];
         }
         __syncthreads();   // the next pair restages the shared inputs
-    }
-    if (t < K) {           // an odd last token, one at a time
-        if (t == acc) store_state();
-        const size_t vec = ((size_t)(n * K + t) * H + h) * D;
-        float kqp = 0.f;
-        if (tid < D) {
-            const float ki = Elem<Tin>::load(k + vec + tid);
-            const float qi = Elem<Tin>::load(q + vec + tid);
-            const float a = __expf(g[vec + tid]);
-            sm.ak[tid] = make_float2(a, ki);
-            sm.kqa[tid] = make_float2(a * ki, a * qi);
-            sm.v[tid] = Elem<Tin>::load(v + vec + tid);
-            kqp = ki * qi;
-        }
-        const float kq = block_sum<C::THREADS>(kqp, sm.red);
-        if (tid == 0) {
-            sm.kq = kq;
-            sm.beta = beta[(size_t)(n * K + t) * H + h];
-        }
-        __syncthreads();
-        float4(&part)[2][C::RG][C::COLG] = *reinterpret_cast<float4(*)[2][C::RG][C::COLG]>(&s_part[0]);
-        token_update<Tin, D>(s, sm, part, r, c, out + vec);
-    }
-    if (acc == K) store_state();
+    };
+    for (int t = 0; t < K; t += 2) pass(t, t + 1 < K);
+    // all K drafts accepted: for odd K the last pass stored it already
+    if (acc == K && (K & 1) == 0) store_state();
 }
 
 template <typename Tin, int D>
@@ -546,9 +550,11 @@ cudaError_t run_verify(const void *q, const void *k, const void *v, const float 
                        const float *beta, const float *state_in, const int32_t *accept,
                        int32_t N, int32_t K, int32_t H, void *out, float *state_out,
                        cudaStream_t stream) {
-    const unsigned units = (unsigned)N * (unsigned)H;
-    if (units == 0) return cudaSuccess;
-    verify_pair_kernel<Tin, D><<<units, DecodeCfg<Tin, D>::THREADS, 0, stream>>>(
+    using C = VerifyCfg<Tin, D>;
+    const uint64_t ctas = (uint64_t)N * (uint64_t)H * C::SPLIT;
+    if (ctas == 0) return cudaSuccess;
+    if (ctas > 0x7fffffffu) return cudaErrorInvalidValue;
+    verify_pair_kernel<Tin, D><<<(unsigned)ctas, C::THREADS, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k), static_cast<const Tin *>(v), g,
         beta, state_in, accept, K, H, static_cast<Tin *>(out), state_out);
     count_launches(1);

@@ -82,6 +82,9 @@ def test_decode_with_warm_conv_cache_and_state(kda):
     (128, torch.float32, 6, [2, 4, 6, 0, 5]),      # even K: every draft in a pair
     (16, torch.bfloat16, 1, [1, 0, 1, 0, 1]),      # one draft: the odd tail alone
     (64, torch.bfloat16, 2, [1, 2, 0, 2, 1]),
+    (128, torch.bfloat16, 1, [1, 0, 1, 0, 1]),     # the odd tail alone, columns split over two CTAs
+    (128, torch.bfloat16, 4, [2, 2, 4, 0, 1]),     # the benchmark's draft count
+    (32, torch.float32, 3, [3, 0, 2, 1, 3]),       # one CTA per (sequence, head)
 ])
 def test_verify_outputs_and_rollback_state(kda, d, dtype, K, accept):
     """K drafts per sequence from a read-only state: all outputs, and the
