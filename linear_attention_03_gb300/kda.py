@@ -130,7 +130,12 @@ def kda_prefill_workspace_size(H: int, d: int, dtype: torch.dtype, T: int, N: in
 
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
                 final_state=None, workspace=None, want_final_state=True):
-    """Chunked prefill over packed documents; returns (out, final_state)."""
+    """Chunked prefill over packed documents; returns (out, final_state).
+
+    workspace: uint8 device tensor, by default kda_prefill_workspace_size
+    bytes (the status word, then the documents' longest-first order when
+    there are several); 256 bytes also work and run the documents in order.
+    """
     T, H, d = q.shape
     dev = q.device
     _dev(q, "q")
