@@ -131,3 +131,44 @@ def test_prologue_argument_checks(kda):
 def test_decode_zero_sequences_is_a_no_op(kda):
     assert kda.lib.kda_decode_step(None, None, None, None, None, None, None, 0,
                                    dims(kda), None) == kda.KDA_OK
+
+
+def test_verify_argument_checks(kda):
+    p, q2 = ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 0x100000)
+    mis = ctypes.c_void_p(FAKE + 4)
+    call = lambda **o: kda.lib.kda_decode_verify(
+        o.get("q", p), p, p, p, p, o.get("sin", p), p, o.get("N", 4), o.get("K", 3),
+        o.get("d", dims(kda)), p, o.get("sout", q2), None)
+    assert call(K=0) == kda.KDA_ERR_INVALID
+    assert call(N=-1) == kda.KDA_ERR_INVALID
+    assert call(N=0) == kda.KDA_OK                              # nothing to do
+    assert call(N=2 ** 24, K=2) == kda.KDA_ERR_INVALID          # N * K * H past 2^31
+    assert call(N=2 ** 24, K=1, d=dims(kda, H=64)) == kda.KDA_ERR_INVALID   # 2 N H past 2^31
+    assert call(q=None) == kda.KDA_ERR_INVALID and "q" in kda.kda_last_error()
+    assert call(q=mis) == kda.KDA_ERR_INVALID
+    assert call(sout=p) == kda.KDA_ERR_INVALID and "alias" in kda.kda_last_error()
+    assert call(d=dims(kda, d=48)) == kda.KDA_ERR_UNSUPPORTED
+
+
+def test_output_gate_argument_checks(kda):
+    p, mis = ctypes.c_void_p(FAKE), ctypes.c_void_p(FAKE + 4)
+    call = lambda **o: kda.lib.kda_output_gate(
+        o.get("o", p), p, o.get("w", None), o.get("T", 64), dims(kda), o.get("eps", 1e-6),
+        o.get("y", p), None)
+    assert call(T=-1) == kda.KDA_ERR_INVALID
+    assert call(T=0) == kda.KDA_OK
+    assert call(eps=-1.0) == kda.KDA_ERR_INVALID
+    assert call(eps=float("nan")) == kda.KDA_ERR_INVALID
+    assert call(o=None) == kda.KDA_ERR_INVALID and "o" in kda.kda_last_error()
+    assert call(y=mis) == kda.KDA_ERR_INVALID
+    assert call(w=mis) == kda.KDA_ERR_INVALID
+
+
+def test_decode_with_conv_cache_argument_checks(kda):
+    p = ctypes.c_void_p(FAKE)
+    call = lambda **o: kda.lib.kda_decode_step_conv(
+        p, p, p, p, o.get("cache", p), p, p, o.get("state", p), p, o.get("N", 8), dims(kda), None)
+    assert call(N=-1) == kda.KDA_ERR_INVALID
+    assert call(N=0) == kda.KDA_OK
+    assert call(cache=None) == kda.KDA_ERR_INVALID and "conv_state" in kda.kda_last_error()
+    assert call(state=None) == kda.KDA_ERR_INVALID and "state" in kda.kda_last_error()
