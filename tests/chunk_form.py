@@ -25,8 +25,12 @@ K3, from first principles", Chapter 6, names without the algebra.
 import numpy as np
 
 
-def chunk_recurrence(q, k, v, g, beta, S0, C):
-    """One head, one document.  q,k,g: [T, dk]; v: [T, dv]; beta: [T]."""
+def chunk_recurrence(q, k, v, g, beta, S0, C, reassociated=False):
+    """One head, one document.  q,k,g: [T, dk]; v: [T, dv]; beta: [T].
+
+    reassociated=True takes U = Tb (V - K+ S0) with Tb = (I+L)^-1 diag(beta)
+    (the order the CUDA prefill computes it in: the state products first,
+    then one product with Tb) instead of Ut - W S0."""
     T = q.shape[0]
     S = np.array(S0, dtype=np.float64, copy=True)
     out = np.zeros((T, v.shape[1]))
@@ -38,11 +42,82 @@ def chunk_recurrence(q, k, v, g, beta, S0, C):
         b = beta[sl][:, None]
         L = np.tril(b * (Kp @ Km.T), -1)
         A = np.eye(n) + L
-        W = np.linalg.solve(A, b * Kp)
-        Ut = np.linalg.solve(A, b * v[sl])
-        U = Ut - W @ S
+        if reassociated:
+            Tb = np.linalg.solve(A, np.diag(beta[sl]))
+            U = Tb @ (v[sl] - Kp @ S)
+        else:
+            W = np.linalg.solve(A, b * Kp)
+            Ut = np.linalg.solve(A, b * v[sl])
+            U = Ut - W @ S
         P = np.tril(Qp @ Km.T)
         out[sl] = Qp @ S + P @ U
         Khat = np.exp(G[-1] - G) * k[sl]
         S = np.exp(G[-1])[:, None] * S + Khat.T @ U
     return out, S
+
+
+def gram_tiled(k, q, g, beta, tile=16):
+    """L and P of one chunk through per-tile reference points, the way the
+    CUDA prefill forms its Gram operands so that every factor stays inside
+    fp32 range.  k, q, g: [C, dk] (C a multiple of `tile`); beta: [C].
+
+    Row tile a (tokens of tile a) uses its start s_a = G before the tile:
+    left rows k_i e^{G_i - s_a} (and q_i e^{G_i - s_a}).  A column token j of
+    tile b <= a uses its tile's end e_b = G after tile b: k_j e^{e_b - G_j},
+    times e^{s_a - e_b} per channel.  The product of the three factors is
+    e^{G_i - G_j}, so L = strict_lower(diag(beta) K+ K-^T) and
+    P = lower_with_diagonal(Q+ K-^T) come out unchanged.  Returns (L, P, the
+    largest factor used)."""
+    C, dk = k.shape
+    G = np.cumsum(g, axis=0)
+    start = np.vstack([np.zeros((1, dk)), G[tile - 1:-1:tile]])   # s_a, one row per tile
+    end = G[tile - 1::tile]                                         # e_b
+    L, P = np.zeros((C, C)), np.zeros((C, C))
+    biggest = 0.0
+    for a in range(C // tile):
+        rows = slice(a * tile, (a + 1) * tile)
+        left_k = np.exp(G[rows] - start[a]) * k[rows]
+        left_q = np.exp(G[rows] - start[a]) * q[rows]
+        biggest = max(biggest, float(np.exp(G[rows] - start[a]).max()))
+        for b in range(a + 1):
+            cols = slice(b * tile, (b + 1) * tile)
+            f_col = np.exp(end[b] - G[cols])
+            f_pair = np.exp(start[a] - end[b])
+            biggest = max(biggest, float(f_col.max()), float(f_pair.max()))
+            right = f_col * f_pair * k[cols]
+            L[rows, cols] = left_k @ right.T
+            P[rows, cols] = left_q @ right.T
+    return np.tril(beta[:, None] * L, -1), np.tril(P), biggest
+
+
+def verify_pairs(q, k, v, g, beta, S0):
+    """Draft tokens two per pass, the algebra of the CUDA verify kernel.
+    One head; q, k, g: [K, dk]; v: [K, dv]; beta: [K].  For tokens t, t+1:
+
+        a_t = (alpha_t k_t)^T S,  b_t = (alpha_t q_t)^T S
+        u_t = beta_t (v_t - a_t),  o_t = b_t + u_t (k_t . q_t)
+        (D_{t+1} S_t)^T x = (alpha_{t+1} alpha_t x)^T S + ((alpha_{t+1} x) . k_t) u_t
+
+    for x = k_{t+1} (its error term) and x = q_{t+1} (its read), with S the
+    state before token t; then S <- D_{t+1} (D_t S + k_t u_t^T) + k_{t+1} u_{t+1}^T.
+    An odd last token runs alone.  Returns (outputs [K, dv], final state)."""
+    S = np.array(S0, dtype=np.float64, copy=True)
+    K = q.shape[0]
+    out = np.zeros((K, v.shape[1]))
+    t = 0
+    while t < K:
+        a1 = np.exp(g[t])
+        u1 = beta[t] * (v[t] - (a1 * k[t]) @ S)
+        out[t] = (a1 * q[t]) @ S + u1 * (k[t] @ q[t])
+        if t + 1 == K:
+            S = a1[:, None] * S + np.outer(k[t], u1)
+            break
+        a2 = np.exp(g[t + 1])
+        e2 = (a2 * a1 * k[t + 1]) @ S + ((a2 * k[t + 1]) @ k[t]) * u1
+        r2 = (a2 * a1 * q[t + 1]) @ S + ((a2 * q[t + 1]) @ k[t]) * u1
+        u2 = beta[t + 1] * (v[t + 1] - e2)
+        out[t + 1] = r2 + u2 * (k[t + 1] @ q[t + 1])
+        S = a2[:, None] * (a1[:, None] * S + np.outer(k[t], u1)) + np.outer(k[t + 1], u2)
+        t += 2
+    return out, S
+

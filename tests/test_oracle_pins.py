@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from tests.chunk_form import chunk_recurrence
+from tests.chunk_form import chunk_recurrence, gram_tiled, verify_pairs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -339,6 +339,62 @@ def test_chunkwise_form_matches_recurrence(C):
         o, f = chunk_recurrence(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], S0[0, h], C)
         close(o, out[:, h], rtol=1e-9, atol=1e-10)
         close(f, fin[0, h], rtol=1e-9, atol=1e-10)
+
+
+@pytest.mark.parametrize("C", [16, 64])
+def test_reassociated_chunk_form_matches_recurrence(C):
+    """U = Tb (V - K+ S0), the order the CUDA prefill computes it in (state
+    products first, then one product with Tb = (I+L)^-1 diag(beta)), equals
+    the pages' Ut - W S0 and the token recurrence to fp64 rounding."""
+    rng = np.random.default_rng(30 + C)
+    T, H, dk, dv = 150, 2, 16, 8
+    q, k, v, g, beta = rand_inputs(rng, T, H, dk, dv)
+    S0 = 0.1 * rng.standard_normal((1, H, dk, dv))
+    out, fin = oracle.recurrence(q, k, v, g, beta, S0)
+    for h in range(H):
+        o, f = chunk_recurrence(q[:, h], k[:, h], v[:, h], g[:, h], beta[:, h], S0[0, h], C,
+                                reassociated=True)
+        close(o, out[:, h], rtol=1e-9, atol=1e-10)
+        close(f, fin[0, h], rtol=1e-9, atol=1e-10)
+
+
+def test_tiled_gram_matches_direct_and_stays_in_fp32_range():
+    """The per-tile reference points of the CUDA prefill's Gram (16-token
+    tiles of a 64-token chunk) give L and P unchanged, and with the bounded
+    gate (g > -5 per token and channel, Kimi K3's lower-bounded decay) no
+    factor exceeds e^(5 x 16) = e^80, inside fp32 range (about e^88.7) --
+    while the direct factors e^{-G} of a whole chunk reach e^320."""
+    rng = np.random.default_rng(41)
+    C, dk = 64, 32
+    k = rng.standard_normal((C, dk)); k /= np.linalg.norm(k, axis=1, keepdims=True)
+    q = rng.standard_normal((C, dk)); q /= np.linalg.norm(q, axis=1, keepdims=True)
+    beta = 1 / (1 + np.exp(-rng.standard_normal(C)))
+    for g in (-5 / (1 + np.exp(-rng.standard_normal((C, dk)))),      # the workloads' gate
+              np.full((C, dk), -5 + 1e-9)):                           # at the bound
+        G = np.cumsum(g, axis=0)
+        Kp, Km, Qp = np.exp(G) * k, np.exp(-G) * k, np.exp(G) * q
+        L_ref = np.tril(beta[:, None] * (Kp @ Km.T), -1)
+        P_ref = np.tril(Qp @ Km.T)
+        L, P, biggest = gram_tiled(k, q, g, beta)
+        close(L, L_ref, rtol=1e-10, atol=1e-12)
+        close(P, P_ref, rtol=1e-10, atol=1e-12)
+        assert biggest <= np.exp(80.0) < np.finfo(np.float32).max
+    assert np.exp(-G).max() > np.exp(300)                               # why the tiles exist
+
+
+@pytest.mark.parametrize("K", [1, 2, 5, 6])
+def test_two_drafts_per_pass_match_recurrence(K):
+    """The verify kernel's pass over the state for two draft tokens at once
+    (the second token's sums expanded over the state before the first) gives
+    the token recurrence's outputs and state; an odd last token alone."""
+    rng = np.random.default_rng(50 + K)
+    dk, dv = 16, 8
+    q, k, v, g, beta = rand_inputs(rng, K, 1, dk, dv)
+    S0 = 0.1 * rng.standard_normal((1, 1, dk, dv))
+    out, fin = oracle.recurrence(q, k, v, g, beta, S0)
+    o, f = verify_pairs(q[:, 0], k[:, 0], v[:, 0], g[:, 0], beta[:, 0], S0[0, 0])
+    close(o, out[:, 0], rtol=1e-11, atol=1e-13)
+    close(f, fin[0, 0], rtol=1e-11, atol=1e-13)
 
 
 # ---------------------------------------------------------------- prologue
