@@ -121,3 +121,46 @@ def verify_pairs(q, k, v, g, beta, S0):
         t += 2
     return out, S
 
+
+
+def block_inverse(L, tile=16):
+    """T = (I + L)^-1 for a strictly lower 64 x 64 L, in the stages of the
+    CUDA prefill (16 x 16 blocks, a, b = 0..3).  With N = I + L split into
+    its diagonal blocks and the rest, D = the inverses of the diagonal blocks
+    (forward substitution) and M = N_offdiag D (strictly block lower, M^4 = 0):
+
+        T = D (I + M)^-1 = D (I - M + M^2 - M^3)
+
+    stage 1: the six M_ab = L_ab D_bb;
+    stage 2: T_{a,a-1} = -D_aa M_{a,a-1},  V20 = M21 M10 - M20,
+             V31 = M32 M21 - M31,  Y30 = M31 M10 - M30;
+    stage 3: T20 = D22 V20,  T31 = D33 V31,  T30 = D33 Y30 + T32 V20."""
+    n = L.shape[0]
+    nb = n // tile
+    assert nb == 4
+    blk = lambda X, a, b: X[a * tile:(a + 1) * tile, b * tile:(b + 1) * tile]
+    D = []
+    for a in range(nb):                          # forward substitution per diagonal block
+        Na = np.eye(tile) + blk(L, a, a)
+        Da = np.zeros((tile, tile))
+        for i in range(tile):
+            Da[i, i] = 1.0
+            for j in range(i):
+                Da[i, j] = -sum(Na[i, m] * Da[m, j] for m in range(j, i))
+        D.append(Da)
+    M = {(a, b): blk(L, a, b) @ D[b] for a in range(nb) for b in range(a)}
+    T = np.zeros((n, n))
+    put = lambda a, b, X: T.__setitem__((slice(a * tile, (a + 1) * tile),
+                                         slice(b * tile, (b + 1) * tile)), X)
+    for a in range(nb):
+        put(a, a, D[a])
+    for a in range(1, nb):
+        put(a, a - 1, -D[a] @ M[a, a - 1])
+    V20 = M[2, 1] @ M[1, 0] - M[2, 0]
+    V31 = M[3, 2] @ M[2, 1] - M[3, 1]
+    Y30 = M[3, 1] @ M[1, 0] - M[3, 0]
+    put(2, 0, D[2] @ V20)
+    put(3, 1, D[3] @ V31)
+    T32 = -D[3] @ M[3, 2]
+    put(3, 0, D[3] @ Y30 + T32 @ V20)
+    return T

@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from tests.chunk_form import chunk_recurrence, gram_tiled, verify_pairs
+from tests.chunk_form import block_inverse, chunk_recurrence, gram_tiled, verify_pairs
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -380,6 +380,24 @@ def test_tiled_gram_matches_direct_and_stays_in_fp32_range():
         close(P, P_ref, rtol=1e-10, atol=1e-12)
         assert biggest <= np.exp(80.0) < np.finfo(np.float32).max
     assert np.exp(-G).max() > np.exp(300)                               # why the tiles exist
+
+
+def test_block_inverse_stages_match_the_inverse():
+    """The prefill's block inverse of I + L (diagonal blocks by forward
+    substitution, then the three stages of products) equals the matrix
+    inverse, for the L of a chunk with the workloads' distributions and for a
+    denser one."""
+    rng = np.random.default_rng(61)
+    C, dk = 64, 32
+    for scale in (1.0, 3.0):
+        k = rng.standard_normal((C, dk)); k /= np.linalg.norm(k, axis=1, keepdims=True)
+        g = -5 / (1 + np.exp(-rng.standard_normal((C, dk)))) / scale
+        beta = 1 / (1 + np.exp(-rng.standard_normal(C)))
+        G = np.cumsum(g, axis=0)
+        L = np.tril(beta[:, None] * ((np.exp(G) * k) @ (np.exp(-G) * k).T), -1)
+        T = block_inverse(L)
+        close(T, np.linalg.inv(np.eye(C) + L), rtol=1e-9, atol=1e-11)
+        close(T @ (np.eye(C) + L), np.eye(C), rtol=0, atol=1e-10)
 
 
 @pytest.mark.parametrize("K", [1, 2, 5, 6])
