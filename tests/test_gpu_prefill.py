@@ -138,3 +138,19 @@ def test_longest_first_dispatch_changes_no_result(kda, d, dtype):
     assert sorted(order) == list(range(N))
     chunks = [-(-lengths[n] // 64) for n in order]
     assert chunks == sorted(chunks, reverse=True)
+
+
+@pytest.mark.parametrize("d,dtype", [(128, torch.bfloat16), (64, torch.float32)])
+def test_weak_decay_reaches_every_block(kda, d, dtype):
+    """Decay 500 times weaker than the workloads' (g in (-0.01, 0), close to
+    DeltaNet): tokens a whole chunk apart still interact, so every block of
+    the chunk's (I + L)^-1 and every Gram tile pairing counts in the outputs
+    (under the workloads' decay the far blocks weigh about e^-40)."""
+    lengths = [320, 75]
+    inp = synth.custom(sum(lengths), 3, d, dtype, seed=470 + d, lengths=lengths,
+                       init_std=0.05, g_scale=0.002)
+    assert float(inp["g"].min()) > -0.0101
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, dtype, f"weak-decay out d={d}")
+    compare(fin, ref_fin, dtype, f"weak-decay state d={d}")
