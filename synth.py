@@ -204,9 +204,10 @@ def inputs(index: int, heads=None, device=None) -> dict:
 
 
 def custom(T, H, d, dtype=torch.float32, seed=100, lengths=None, init_std=0.0,
-           unit_qk=True, g_scale=1.0):
+           unit_qk=True, g_scale=1.0, g_const=None):
     """Small ad-hoc inputs with the workload distributions (edge-case tests);
-    g_scale < 1 draws a weaker decay, g = g_scale * gmin * sigmoid(N(0,1))."""
+    g_scale < 1 draws a weaker decay, g = g_scale * gmin * sigmoid(N(0,1));
+    g_const fills every g with one value instead (a degenerate case)."""
     lengths = [T] if lengths is None else list(lengths)
     assert sum(lengths) == T
     res = {"cu_seqlens": cu_seqlens_of(lengths)}
@@ -215,7 +216,8 @@ def custom(T, H, d, dtype=torch.float32, seed=100, lengths=None, init_std=0.0,
     res["k"] = _heads_tensor(H, None, lambda h: qd(_normal(seed, K, h, (T, d))), dtype)
     res["v"] = _heads_tensor(H, None, lambda h: _normal(seed, V, h, (T, d)), dtype)
     res["g"] = _heads_tensor(H, None,
-                             lambda h: g_scale * _log_decay(_normal(seed, ZG, h, (T, d))),
+                             lambda h: g_scale * _log_decay(_normal(seed, ZG, h, (T, d)))
+                             if g_const is None else np.full((T, d), g_const),
                              torch.float32)
     res["beta"] = _heads_tensor(H, None, lambda h: _logistic(_normal(seed, ZB, h, (T, 1))),
                                 torch.float32)[..., 0].contiguous()

@@ -154,3 +154,18 @@ def test_weak_decay_reaches_every_block(kda, d, dtype):
     ref_out, ref_fin = oracle_prefill(inp)
     compare(out, ref_out, dtype, f"weak-decay out d={d}")
     compare(fin, ref_fin, dtype, f"weak-decay state d={d}")
+
+
+def test_gate_at_its_bound(kda):
+    """Every g just above the bounded gate's floor of -5 (Kimi K3's
+    lower-bounded decay): the tensor-core prefill's 16-token rescaling
+    factors reach their e^80 limit, inside fp32 range, and the results still
+    match the oracle."""
+    lengths = [200, 64]
+    inp = synth.custom(sum(lengths), 3, 128, torch.bfloat16, seed=480, lengths=lengths,
+                       init_std=0.05, g_const=-5.0 + 1e-6)
+    assert float(inp["g"].min()) >= -5.0
+    out, fin = gpu_prefill(kda, to_device(inp))
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, torch.bfloat16, "gate at its bound, out")
+    compare(fin, ref_fin, torch.bfloat16, "gate at its bound, state")
