@@ -164,3 +164,38 @@ def block_inverse(L, tile=16):
     T32 = -D[3] @ M[3, 2]
     put(3, 0, D[3] @ Y30 + T32 @ V20)
     return T
+
+
+def segmented_three_pass(q, k, v, g, beta, S0, nseg, prefill):
+    """One document as `nseg` segments of whole 64-token chunks, joined the
+    way the segment-scan prefill joins them (test-only; `prefill` is any
+    exact single-document prefill, here the oracle's recurrence).  The
+    recurrence is linear in (v, S_in), and over a segment S_out = P S_in + R:
+      1. v as given, segment 0 from S0, the others from zero: outputs o^0, R_s;
+      2. v = 0 from the identity: P_s;
+      3. S_1 = R_0, S_{s+1} = P_s S_s + R_s;
+      4. v = 0 from S_s: the outputs the incoming state adds, o = o^0 + o^S.
+    Shapes as the oracle's: q, k, g [T, H, d]; v [T, H, d]; S0 [1, H, d, d]."""
+    T, H, d = q.shape
+    chunks = -(-T // 64)
+    seg_len = -(-chunks // nseg) * 64
+    bounds = [(s0, min(s0 + seg_len, T)) for s0 in range(0, T, seg_len)]
+    out = np.zeros_like(v, dtype=np.float64)
+    eye = np.broadcast_to(np.eye(d), (1, H, d, d)).copy()
+    zero_state = np.zeros((1, H, d, d))
+    R, P = [], []
+    for i, (a, b) in enumerate(bounds):
+        sl = slice(a, b)
+        o0, r = prefill(q[sl], k[sl], v[sl], g[sl], beta[sl], S0 if i == 0 else zero_state)
+        _, p = prefill(q[sl], k[sl], np.zeros_like(v[sl]), g[sl], beta[sl], eye)
+        out[sl] = o0
+        R.append(r)
+        P.append(p)
+    S = R[0]
+    for i in range(1, len(bounds)):
+        a, b = bounds[i]
+        sl = slice(a, b)
+        oS, _ = prefill(q[sl], k[sl], np.zeros_like(v[sl]), g[sl], beta[sl], S)
+        out[sl] += oS
+        S = np.einsum("hij,hjk->hik", P[i][0], S[0])[None] + R[i]
+    return out, S

@@ -15,7 +15,8 @@ import pytest
 import torch
 
 import oracle
-from tests.chunk_form import block_inverse, chunk_recurrence, gram_tiled, verify_pairs
+from tests.chunk_form import (block_inverse, chunk_recurrence, gram_tiled,
+                              segmented_three_pass, verify_pairs)
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -402,6 +403,24 @@ def test_block_inverse_stages_match_the_inverse():
         T = block_inverse(L)
         close(T, np.linalg.inv(np.eye(C) + L), rtol=1e-9, atol=1e-11)
         close(T @ (np.eye(C) + L), np.eye(C), rtol=0, atol=1e-10)
+
+
+@pytest.mark.parametrize("nseg", [1, 2, 3, 5])
+def test_segment_scan_three_prefills_match_recurrence(nseg):
+    """The segment-scan prefill's decomposition (three prefills of the
+    segments as independent documents, then the scan of their affine maps,
+    From GPT-2 to Kimi K3, Chapter 6, context parallelism) gives the
+    one-document recurrence's outputs and final state, with an initial state
+    and a ragged last segment."""
+    rng = np.random.default_rng(70 + nseg)
+    T, H, d = 300, 2, 8
+    q, k, v, g, beta = rand_inputs(rng, T, H, d, d, g_scale=0.05)   # a slow decay: segments interact
+    S0 = 0.1 * rng.standard_normal((1, H, d, d))
+    out, fin = oracle.recurrence(q, k, v, g, beta, S0)
+    prefill = lambda *a: oracle.recurrence(*a)
+    o, f = segmented_three_pass(q, k, v, g, beta, S0, nseg, prefill)
+    close(o, out, rtol=1e-9, atol=1e-11)
+    close(f, fin, rtol=1e-9, atol=1e-11)
 
 
 @pytest.mark.parametrize("K", [1, 2, 5, 6])
