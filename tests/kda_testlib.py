@@ -3,12 +3,14 @@ binding, run the fp64 oracle on the same inputs, compare.
 
 Tolerances (written here once, used by every parity test):
   * fp32 inputs: max |gpu - oracle| <= 1e-4 (absolute), outputs and states.
-  * bf16 inputs, fp32 state: RMS(gpu - oracle) <= 2e-2 * RMS(oracle) ("2e-2
-    relative to output RMS"), and in addition max |gpu - oracle| <= 2e-2 *
-    max |oracle|, separately for the outputs and for the final states.
-    A max-abs error held to 2e-2 * RMS cannot be met by any bf16 output:
-    rounding an output to bf16 alone costs up to 2^-8 of its magnitude, and
-    the largest outputs reach ~12x the RMS (measured on the smoke inputs).
+  * bf16 inputs, fp32 state ("2e-2 relative to output RMS"):
+      - RMS(gpu - oracle) <= 2e-2 * RMS(oracle), for outputs and states;
+      - every element of an fp32 result (the final states, the gates):
+        |gpu - oracle| <= 2e-2 * RMS(oracle);
+      - every element of a bf16 result (the outputs):
+        |gpu - oracle| <= 2e-2 * RMS(oracle) + half a bf16 ulp of the oracle
+        value, the rounding that storing it in bf16 costs by itself (the
+        largest outputs reach ~12x the RMS, where that half ulp is ~0.02 x RMS).
 """
 import numpy as np
 import torch
@@ -31,8 +33,21 @@ def rms(x):
     return float(np.sqrt(np.mean(np.square(x)))) if x.size else 0.0
 
 
+def half_ulp_bf16(x):
+    """Half the spacing of bf16 numbers at |x| (bf16 keeps 8 significant bits)."""
+    _, e = np.frexp(np.abs(x))          # |x| = m 2^e with m in [0.5, 1)
+    return np.where(x == 0, 0.0, np.ldexp(1.0, e - 9))
+
+
+LAST = {}   # the last comparison's relative errors, by label (printed with -s)
+
+
 def compare(got, ref, dtype, what):
-    """Assert parity under the tolerance of `dtype`; return (max_err, bound)."""
+    """Assert parity under the tolerance of `dtype`; return (rel_rms, max_rel).
+
+    `got` is the GPU result as it was stored (a bf16 tensor is an output that
+    was rounded to bf16 once); `ref` the fp64 oracle value."""
+    rounded = isinstance(got, torch.Tensor) and got.dtype == torch.bfloat16
     got, ref = f64(got), f64(ref)
     assert got.shape == ref.shape, (what, got.shape, ref.shape)
     assert np.all(np.isfinite(got)), f"{what}: non-finite values"
@@ -44,12 +59,37 @@ def compare(got, ref, dtype, what):
         bound = TOL_F32_ABS
         assert err <= bound, f"{what}: max|err| = {err:.3e} > {bound:.3e}"
         return err, bound
-    rel = rms(diff) / max(rms(ref), 1e-30)
+    r = max(rms(ref), 1e-30)
+    rel = rms(diff) / r
+    LAST[what] = (rel, err / r)
     assert rel <= TOL_BF16_REL_RMS, \
         f"{what}: RMS(err)/RMS(ref) = {rel:.3e} > {TOL_BF16_REL_RMS:.0e}"
-    bound = TOL_BF16_REL_RMS * float(np.abs(ref).max())
-    assert err <= bound, f"{what}: max|err| = {err:.3e} > 2e-2 * max|ref| = {bound:.3e}"
-    return rel, TOL_BF16_REL_RMS
+    bound = TOL_BF16_REL_RMS * r + (half_ulp_bf16(ref) if rounded else 0.0)
+    over = diff > bound
+    if over.any():
+        i = np.unravel_index(int(np.argmax(diff - bound)), diff.shape)
+        raise AssertionError(
+            f"{what}: {int(over.sum())} elements above the element bound; worst at {i}: "
+            f"|err| = {diff[i]:.3e}, bound {np.broadcast_to(bound, diff.shape)[i]:.3e} "
+            f"(2e-2 RMS = {TOL_BF16_REL_RMS * r:.3e}{', + half a bf16 ulp' if rounded else ''})")
+    print(f"[parity] {what}: rel RMS {rel:.2e}, max|err|/RMS {err / r:.2e}")
+    return rel, err / r
+
+
+def as_stored(x, dtype):
+    """Round fp64 values to the dtype they are stored in between two operators:
+    the prologue's q, k, v are tensors of the workload's qkv dtype, its gates
+    fp32, and the prefill consumes exactly those values."""
+    t = torch.from_numpy(np.ascontiguousarray(x))
+    return t.to(dtype).to(torch.float64).numpy()
+
+
+def oracle_prologue_stored(prologue_out, dtype):
+    """oracle.prologue's (q, k, v, g, beta) as the prefill receives them: q, k, v
+    in `dtype`, g and beta in fp32 (None stays None)."""
+    q, k, v, g, b = prologue_out
+    r = lambda x, dt: None if x is None else as_stored(x, dt)
+    return r(q, dtype), r(k, dtype), r(v, dtype), r(g, torch.float32), r(b, torch.float32)
 
 
 def oracle_prefill(inp, heads=None, threads=0):

@@ -5,7 +5,7 @@ import torch
 
 import oracle
 import synth
-from tests.kda_testlib import compare, f64, gpu_prefill, oracle_prefill, to_device
+from tests.kda_testlib import compare, f64, oracle_prologue_stored, gpu_prefill, oracle_prefill, to_device
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
@@ -102,7 +102,10 @@ def test_prologue_without_gates(kda):
 
 def test_prologue_then_prefill(kda):
     """The fused input path feeding the prefill, against oracle prologue +
-    oracle recurrence (the long-context workload's pipeline, small)."""
+    oracle recurrence (the long-context workload's pipeline, small).  The
+    prologue hands q, k, v to the prefill as bf16 tensors (the interface's
+    qkv dtype), so the reference recurrence takes the oracle prologue's
+    values rounded the same way."""
     lengths = [90, 0, 71]
     T = sum(lengths)
     inp = synth.custom_raw(T, 3, 128, torch.bfloat16, seed=730, lengths=lengths)
@@ -111,7 +114,7 @@ def test_prologue_then_prefill(kda):
     q, k, v, g, b = kda.kda_prologue(dv["q_raw"], dv["k_raw"], dv["v_raw"], dv["conv_w"],
                                      dv["z_g"], dv["z_beta"], cu)
     out, fin = kda.kda_prefill(q, k, v, g, b, None, cu)
-    rq, rk, rv, rg, rb = _prologue_ref(inp)
+    rq, rk, rv, rg, rb = oracle_prologue_stored(_prologue_ref(inp), torch.bfloat16)
     ref_out, ref_fin = oracle.recurrence(rq, rk, rv, rg, rb, None, inp["cu_seqlens"])
     compare(out, ref_out, torch.bfloat16, "prologue+prefill out")
     compare(fin, ref_fin, torch.bfloat16, "prologue+prefill state")

@@ -11,7 +11,7 @@ import torch
 
 import oracle
 import synth
-from tests.kda_testlib import compare, f64, to_device
+from tests.kda_testlib import compare, f64, oracle_prologue_stored, to_device
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
@@ -25,9 +25,11 @@ def check(kda, T, H, d, dtype, seg, seed, with_state):
     out, fin = kda.kda_prologue_prefill(dv["q_raw"], dv["k_raw"], dv["v_raw"], dv["conv_w"],
                                         dv["z_g"], dv["z_beta"],
                                         None if s0 is None else s0.cuda(), seg)
-    rq, rk, rv, rg, rb = oracle.prologue(f64(raw["q_raw"]), f64(raw["k_raw"]), f64(raw["v_raw"]),
-                                         f64(raw["conv_w"]), f64(raw["z_g"]), f64(raw["z_beta"]),
-                                         raw["cu_seqlens"])
+    # the prologue stores q, k, v in the qkv dtype before the prefill reads them
+    rq, rk, rv, rg, rb = oracle_prologue_stored(
+        oracle.prologue(f64(raw["q_raw"]), f64(raw["k_raw"]), f64(raw["v_raw"]),
+                        f64(raw["conv_w"]), f64(raw["z_g"]), f64(raw["z_beta"]), raw["cu_seqlens"]),
+        dtype)
     ref_out, ref_fin = oracle.recurrence(rq, rk, rv, rg, rb,
                                          None if s0 is None else f64(s0)[None], raw["cu_seqlens"])
     compare(out, ref_out, dtype, f"pipeline out T={T} seg={seg}")

@@ -42,7 +42,7 @@ def test_segmented_other_heads_match_oracle(kda, d, dtype):
     compare(fin, ref_fin[0], dtype, f"segmented state d={d}")
 
 
-def test_segmented_from_zero_state_and_equal_to_plain_prefill(kda):
+def test_segmented_and_plain_prefill_from_zero_state(kda):
     T = 2048
     inp = synth.custom(T, 4, 128, torch.bfloat16, seed=970)
     out, fin = run(kda, inp, 5)
@@ -51,7 +51,8 @@ def test_segmented_from_zero_state_and_equal_to_plain_prefill(kda):
     compare(fin, ref_fin[0], torch.bfloat16, "segmented state, zero state")
     dv = to_device(inp)
     plain_out, plain_fin = kda.kda_prefill(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"])
-    compare(out, plain_out.cpu().double().numpy(), torch.bfloat16, "segmented vs plain out")
+    compare(plain_out, ref_out, torch.bfloat16, "plain out, zero state")
+    compare(plain_fin, ref_fin, torch.bfloat16, "plain state, zero state")
 
 
 def test_segmented_empty_document_keeps_the_state(kda):

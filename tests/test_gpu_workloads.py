@@ -9,7 +9,7 @@ import torch
 
 import oracle
 import synth
-from tests.kda_testlib import compare, f64, gpu_prefill, oracle_prefill, to_device
+from tests.kda_testlib import compare, f64, gpu_prefill, oracle_prefill, oracle_prologue_stored, to_device
 
 pytestmark = [pytest.mark.gpu,
               pytest.mark.skipif(not torch.cuda.is_available(), reason="needs a GPU")]
@@ -58,7 +58,8 @@ def test_workload4_long_context_with_prologue(kda):
     compare(v[:, heads], rv, torch.bfloat16, "w4 prologue v")
     compare(g[:, heads], rg, torch.float32, "w4 prologue g")
     compare(b[:, heads], rb, torch.float32, "w4 prologue beta")
-    ref_out, ref_fin = oracle.recurrence(rq, rk, rv, rg, rb)
+    # the prefill reads the prologue's q, k, v as stored (bf16) and g, beta (fp32)
+    ref_out, ref_fin = oracle.recurrence(*oracle_prologue_stored((rq, rk, rv, rg, rb), torch.bfloat16))
     compare(out[:, heads], ref_out, torch.bfloat16, "w4 out (sampled heads)")
     compare(fin[:, heads], ref_fin, torch.bfloat16, "w4 state (sampled heads)")
     assert out.shape == (T, 96, 128)
