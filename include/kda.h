@@ -75,6 +75,9 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 #define KDA_DEVICE_OK 0
 #define KDA_DEVICE_BAD_OFFSETS 1  /* cu_seqlens not 0..T and non-decreasing */
 #define KDA_DEVICE_TIMEOUT 2      /* a bounded device-side wait ran out      */
+#define KDA_DEVICE_RANGE 3        /* a value the tensor-core prefill keeps in fp16 operands (v, the
+                                     state, the pseudo-values) reached 65504 in magnitude: the
+                                     results of that call are not valid                          */
 
 typedef struct {
     int32_t H;          /* heads                                   */

@@ -398,6 +398,8 @@ kda_status kda_get_device_status(const void *workspace, int32_t *status_out,
     if (word == KDA_DEVICE_OK) return KDA_OK;
     if (word == KDA_DEVICE_TIMEOUT)
         return fail(KDA_ERR_TIMEOUT, "a device-side wait gave up%s");
+    if (word == KDA_DEVICE_RANGE)
+        return fail(KDA_ERR_DEVICE, "a value held in fp16 operands reached 65504 in magnitude%s");
     return fail(KDA_ERR_DEVICE, "the device rejected cu_seqlens (not 0..T, non-decreasing)%s");
 }
 

@@ -155,13 +155,15 @@ cudaError_t launch_output_gate(const void *o, const void *z, const float *weight
 
 cudaError_t launch_selftest_wait(uint64_t limit_ns, int32_t *status, cudaStream_t stream);
 
-// Tensor-core chunked prefill (d = 128, bf16 q/k/v).
+// Tensor-core chunked prefill (d = 128, bf16 q/k/v).  With out_f32 set, the
+// outputs go there in fp32 (and `out` is not written).
 bool chunk_prefill_supported(int32_t D, kda_dtype dt);
 cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, const float *g,
                                  const float *beta, const float *init_state,
                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
                                  void *out, float *final_state, int32_t *status,
-                                 cudaStream_t stream, const int32_t *order = nullptr);
+                                 cudaStream_t stream, const int32_t *order = nullptr,
+                                 float *out_f32 = nullptr);
 
 // prologue and prefill of one document, segment by segment, overlapped
 size_t pipeline_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int64_t segment_tokens);

@@ -110,24 +110,14 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
         : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
     return *reinterpret_cast<float2 *>(&d);
 }
-__device__ __forceinline__ float tanh_approx(float x) {
-    float t;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(t) : "f"(x));
-    return t;
-}
-
-// Swish s = y sigmoid(y) on a pair.  For bf16 outputs it is
-// 0.5 y (1 + tanh(y / 2)) on the hardware tanh (one special-function op
-// instead of an exponential and a reciprocal; its ~5e-4 error is below the
-// bf16 rounding of s); fp32 outputs keep y / (1 + e^-y).
+// Swish s = y sigmoid(y) on a pair, y / (1 + e^-y) for either output type.
+// (The hardware tanh form 0.5 y (1 + tanh(y / 2)), one special-function op,
+// has an error of ~5e-4 of s: below bf16's rounding step, but it moves about
+// one bf16 rounding in sixteen to the neighbouring value, and the prefill
+// carries those changed inputs into every later output.)
 template <typename Tin>
 __device__ __forceinline__ float2 swish2(float2 y) {
-    if constexpr (std::is_same<Tin, __nv_bfloat16>::value) {
-        const float2 hy = mul2(make_float2(0.5f, 0.5f), y);
-        return fma2(hy, make_float2(tanh_approx(hy.x), tanh_approx(hy.y)), hy);
-    } else {
-        return make_float2(__fdividef(y.x, 1.f + __expf(-y.x)), __fdividef(y.y, 1.f + __expf(-y.y)));
-    }
+    return make_float2(__fdividef(y.x, 1.f + __expf(-y.x)), __fdividef(y.y, 1.f + __expf(-y.y)));
 }
 
 template <typename Tin, int D>

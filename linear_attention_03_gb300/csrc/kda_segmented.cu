@@ -13,6 +13,8 @@
 //   2. v = 0 from the identity: the states P_s;
 //   3. the scan S_1 = R_0, S_{s+1} = P_s S_s + R_s (S_end = final state);
 //   4. v = 0 from S_s: the outputs the incoming state adds, o = o^0 + o^S.
+// With the tensor-core prefill (bf16 q/k/v) o^0 and o^S are kept in fp32 and
+// the sum is rounded to bf16 once.
 // It costs three prefills instead of one, spread over segments x heads CTAs:
 // it pays off when heads x documents alone cannot fill the GPU.
 #include "kda_internal.cuh"
@@ -26,8 +28,11 @@ size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 struct SegLayout {
     int32_t nseg;
     int64_t seg_len;
-    size_t status, cu, v0, init0, ident, R, P, Sin, ocorr, total;
+    size_t status, cu, v0, init0, ident, R, P, Sin, ocorr, o0f, total;
 };
+
+// fp32 partial outputs: the tensor-core prefill (bf16 inputs, d = 128)
+bool f32_partials(int32_t D, kda_dtype dt) { return chunk_prefill_supported(D, dt); }
 
 SegLayout layout(int32_t H, int32_t D, kda_dtype dt, int64_t T, int32_t num_segments) {
     SegLayout L{};
@@ -48,7 +53,9 @@ SegLayout layout(int32_t H, int32_t D, kda_dtype dt, int64_t T, int32_t num_segm
     L.R = off; off += up(st);
     L.P = off; off += up(st);
     L.Sin = off; off += up(st);
-    L.ocorr = off; off += up(tok);
+    const size_t tokf = static_cast<size_t>(T) * H * D * sizeof(float);
+    L.ocorr = off; off += up(f32_partials(D, dt) ? tokf : tok);
+    L.o0f = off; off += f32_partials(D, dt) ? up(tokf) : 0;
     L.total = off;
     return L;
 }
@@ -128,6 +135,19 @@ __global__ void __launch_bounds__(256) seg_scan_kernel(const float *__restrict__
     }
 }
 
+// out = bf16(o^0 + o^S), the partial outputs in fp32
+__global__ void sum_partials_kernel(__nv_bfloat16 *out, const float *o0, const float *os, int64_t n) {
+    const int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (int64_t e = 4 * i; e < n; e += 4 * static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const float4 a = *reinterpret_cast<const float4 *>(o0 + e);
+        const float4 b = *reinterpret_cast<const float4 *>(os + e);
+        __nv_bfloat162 lo = __floats2bfloat162_rn(a.x + b.x, a.y + b.y);
+        __nv_bfloat162 hi = __floats2bfloat162_rn(a.z + b.z, a.w + b.w);
+        *reinterpret_cast<__nv_bfloat162 *>(out + e) = lo;
+        *reinterpret_cast<__nv_bfloat162 *>(out + e + 2) = hi;
+    }
+}
+
 // out += o^S for the tokens after segment 0 (segment 0's correction is zero)
 template <typename T>
 __global__ void add_correction_kernel(T *out, const T *corr, int64_t begin, int64_t n) {
@@ -177,13 +197,16 @@ cudaError_t launch_prefill_segmented(const void *q, const void *k, const void *v
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
 
-    auto prefill = [&](const void *vv, const float *init, void *o, float *fin) {
-        return use_chunk ? launch_prefill_chunk(q, k, vv, g, beta, init, cu, n, T, H, o, fin, status, s)
+    const bool f32p = use_chunk && f32_partials(D, dt);
+    float *o0f = f32p ? reinterpret_cast<float *>(ws + L.o0f) : nullptr;
+    auto prefill = [&](const void *vv, const float *init, void *o, float *fin, float *of) {
+        return use_chunk ? launch_prefill_chunk(q, k, vv, g, beta, init, cu, n, T, H, o, fin, status, s,
+                                                nullptr, of)
                          : launch_prefill_recurrent(q, k, vv, g, beta, init, cu, n, T, H, D, dt, o, fin,
                                                     status, s);
     };
     // 1. outputs from zero state (segment 0 from init_state) and the states R_s
-    if ((e = prefill(v, init0, out, R)) != cudaSuccess) return e;
+    if ((e = prefill(v, init0, out, R, n > 1 ? o0f : nullptr)) != cudaSuccess) return e;
     if (n == 1) {
         if (final_state != nullptr &&
             (e = cudaMemcpyAsync(final_state, R, static_cast<size_t>(H) * mat, cudaMemcpyDeviceToDevice,
@@ -192,7 +215,8 @@ cudaError_t launch_prefill_segmented(const void *q, const void *k, const void *v
         return cudaSuccess;
     }
     // 2. the transition maps P_s (v = 0 from the identity); the outputs are scratch
-    if ((e = prefill(v0, ident, ocorr, P)) != cudaSuccess) return e;
+    if ((e = prefill(v0, ident, ocorr, P, f32p ? static_cast<float *>(ocorr) : nullptr)) != cudaSuccess)
+        return e;
     // 3. the states entering each segment, and the final state
     const size_t scan_smem = 2 * mat;
     switch (D) {
@@ -210,9 +234,13 @@ cudaError_t launch_prefill_segmented(const void *q, const void *k, const void *v
     count_launches(1);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     // 4. what the incoming states add to the outputs (v = 0 from S_s), then the sum
-    if ((e = prefill(v0, Sin, ocorr, nullptr)) != cudaSuccess) return e;
+    if ((e = prefill(v0, Sin, ocorr, nullptr, f32p ? static_cast<float *>(ocorr) : nullptr)) != cudaSuccess)
+        return e;
     const int64_t begin = L.seg_len * H * D, total = T * H * D;
-    if (dt == KDA_BF16)
+    if (f32p)
+        sum_partials_kernel<<<2048, 256, 0, s>>>(static_cast<__nv_bfloat16 *>(out), o0f,
+                                                 static_cast<const float *>(ocorr), total);
+    else if (dt == KDA_BF16)
         add_correction_kernel<__nv_bfloat16><<<2048, 256, 0, s>>>(
             static_cast<__nv_bfloat16 *>(out), static_cast<const __nv_bfloat16 *>(ocorr), begin, total);
     else

@@ -24,7 +24,7 @@ lib = ctypes.CDLL(_LIB_PATH)
 KDA_OK, KDA_ERR_INVALID, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
     KDA_ERR_DEVICE = range(6)
 KDA_F32, KDA_BF16 = 0, 1
-KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT = 0, 1, 2
+KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT, KDA_DEVICE_RANGE = 0, 1, 2, 3
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
            "kda_prologue", "kda_get_device_status", "kda_last_error",
            "kda_kernel_launches", "kda_decode_step_conv", "kda_decode_verify",
