@@ -311,10 +311,15 @@ KDA_API const char *kda_last_error(void);
  * batches run in document order, with the same results.
  *   status_out  device int32 or NULL; receives the device status word
  *               (KDA_DEVICE_*) of this call, in stream order.
- * The first call on each device looks the array's address up (the device
- * must be current) and should come before any stream capture.  Calls share
- * the array: calls that overlap on the GPU race.  Allocates nothing: no
- * cudaMalloc or cudaFree, no allocating library routine.
+ * The first call in each CUDA context looks the array's address up and,
+ * under CUDA's lazy module loading, loads the library's modules (the array
+ * and the prefill kernels) into the context, which takes device memory: make
+ * that first call at start-up, before any stream capture.  Later calls in the
+ * same context allocate nothing: no cudaMalloc or cudaFree, no allocating
+ * library routine.  The address is cached per context ID, so a context
+ * created after cudaDeviceReset (which destroys the old context's copy of
+ * the array) does its own first-call lookup again.  Calls share the array:
+ * calls that overlap on the GPU race.
  */
 KDA_API kda_status kda_prefill_noalloc(const void *q, const void *k, const void *v,
                                        const float *g, const float *beta,
