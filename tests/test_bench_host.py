@@ -46,3 +46,28 @@ def test_traffic_records_point_at_sources_and_scale_with_units(monkeypatch, tmp_
     assert bench.traffic_for("missing", 25) is None
     src.write_text("kernel source, edited\n")
     assert bench.traffic_for("a", 25) is None
+
+
+def test_leg_summaries_close_the_line():
+    """Every leg's value and roofline fraction sit in the last 1.5 KB of the
+    printed line, after the verbose records."""
+    rf = lambda f: {"bound": "hbm", "achieved": 1.0, "peak": 2.0, "unit": "GB/s", "frac": f,
+                    "traffic": None, "algorithmic_bytes": 1}
+    verbose = {"workload": "x" * 400, "roofline": rf(0.5), "note": "y" * 400}
+    dec = dict(verbose, value=2097.9, unit="steps/s", ms_per_step=0.4767, roofline=rf(1.03))
+    lng = dict(verbose, value=1.0e7, unit="tokens/s", ms_per_step=26.0, roofline=rf(0.22),
+               two_kernels={"prologue": {"ms": 3.0}, "prefill": {"ms": 22.1}})
+    ext = {name: dict(verbose, value=1.0, unit="u", ms_per_step=1.0, roofline=rf(0.9))
+           for name in ("decode_conv", "verify", "output_gate", "packed_documents",
+                        "segmented_h8", "segmented_h96")}
+    ext["clocks"] = {"sm_mhz": 2070.0}
+    legs = bench.legs_summary(dec, lng, ext)
+    assert legs["decode"] == {"value": 2097.9, "unit": "steps/s", "ms_per_step": 0.4767, "frac": 1.03}
+    assert legs["long_context"]["prefill_alone_ms"] == 22.1
+    assert legs["packed_documents"]["frac"] == 0.9
+    assert set(legs["extras"]) == {"decode_conv", "verify", "output_gate", "segmented_h8", "segmented_h96"}
+    line = {"metric": "m", "value": 1.0, "detail": {"decode": dec, "long_context": lng, "extras": ext},
+            "legs": legs}
+    tail = json.dumps(line)[-1500:]
+    assert '"decode": {"value": 2097.9' in tail and '"frac": 1.03' in tail
+    assert '"long_context": {"value": 10000000.0' in tail
