@@ -148,14 +148,27 @@ KDA_API size_t kda_prologue_prefill_workspace_size(kda_dims dims, int64_t T, int
  *   out [T, H, d_v] qkv_dtype
  *   workspace  kda_prologue_prefill_workspace_size() bytes, 256-byte aligned;
  *              its first word is the device status word
- * The work runs on two library streams of the current device, after the work
- * already queued on `stream`, and `stream` waits for it.
+ *   stream           the caller's stream: the prefills run on it, and it
+ *                    holds the end of the whole call (results ready in its
+ *                    order)
+ *   prologue_stream  the caller's second stream for the prologues, which
+ *                    start after the work already queued on `stream`; give
+ *                    it a lower priority than `stream` so that the prefill's
+ *                    serial chain is not held back.  The same stream as
+ *                    `stream` runs the segments one after another (no
+ *                    overlap, same results).
+ * Both streams belong to the caller.  The call creates five CUDA events to
+ * order the two streams and destroys them before it returns (CUDA releases
+ * an event once the work it tracks is done); the library keeps no stream,
+ * event or memory from the call.  Calls that share a workspace must not
+ * overlap on the GPU.
  */
 KDA_API kda_status kda_prologue_prefill(const void *q_raw, const void *k_raw, const void *v_raw,
                                         const float *conv_w, const float *z_g, const float *z_beta,
                                         const float *init_state, int64_t T, kda_dims dims,
                                         int64_t segment_tokens, void *out, float *final_state,
-                                        void *workspace, size_t workspace_bytes, void *stream);
+                                        void *workspace, size_t workspace_bytes, void *stream,
+                                        void *prologue_stream);
 
 /*
  * Bytes of device workspace kda_prefill_segmented needs (0 for invalid

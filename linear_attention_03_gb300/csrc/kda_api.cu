@@ -156,7 +156,8 @@ kda_status kda_prologue_prefill(const void *q_raw, const void *k_raw, const void
                                 const float *conv_w, const float *z_g, const float *z_beta,
                                 const float *init_state, int64_t T, kda_dims dims,
                                 int64_t segment_tokens, void *out, float *final_state,
-                                void *workspace, size_t workspace_bytes, void *stream) {
+                                void *workspace, size_t workspace_bytes, void *stream,
+                                void *prologue_stream) {
     g_last_error[0] = '\0';
     KDA_TRY(check_dims(dims));
     if (T < 0 || T > INT32_MAX) return fail(KDA_ERR_INVALID, "T must be in [0, 2^31)%s");
@@ -190,7 +191,8 @@ kda_status kda_prologue_prefill(const void *q_raw, const void *k_raw, const void
     const bool chunk = kda::chunk_prefill_supported(dims.d_k, dt) && !force_recurrent();
     cudaError_t err = kda::launch_prologue_prefill(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, init_state, T,
                                                    dims.H, dims.d_k, dt, segment_tokens, out, final_state,
-                                                   workspace, chunk, s);
+                                                   workspace, chunk, s,
+                                                   static_cast<cudaStream_t>(prologue_stream));
     if (err != cudaSuccess) return cuda_fail(err, "prologue + prefill launch");
     return KDA_OK;
 }

@@ -172,7 +172,7 @@ cudaError_t launch_prologue_prefill(const void *q_raw, const void *k_raw, const 
                                     const float *init_state, int64_t T, int32_t H, int32_t D,
                                     kda_dtype dt, int64_t segment_tokens, void *out,
                                     float *final_state, void *workspace, bool use_chunk,
-                                    cudaStream_t user);
+                                    cudaStream_t user, cudaStream_t pro);
 
 // prefill of one document as independent segments joined by an exact scan
 size_t segmented_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int32_t num_segments);

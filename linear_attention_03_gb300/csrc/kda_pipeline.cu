@@ -7,11 +7,14 @@
 // the prologue, which streams HBM, fills them.  The intermediate q, k, v, g
 // and beta live in two segment-sized buffers instead of T-sized ones.
 //
-// Ordering: two library streams per device, the prefills on the higher
-// priority one.  Both start after the work already queued on the caller's
-// stream, and the caller's stream waits for the last prefill.
-#include <mutex>
-
+// Ordering: the caller owns both streams.  The prefills run on the caller's
+// `stream`, the prologues on `pro` (the caller's second stream, normally of
+// lower priority); `pro` starts after the work already queued on `stream`, and
+// since the last prefill waits for the last prologue, `stream` holds the end
+// of the whole call.  The cross-stream events are created by the call and
+// destroyed before it returns (CUDA releases them once their work is done),
+// so nothing outlives the call.  With pro == stream the segments run one
+// after another.
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -44,34 +47,21 @@ int64_t seg_tokens_of(int64_t T, int64_t segment_tokens) {
     return T > 0 && L > T ? (T + 63) / 64 * 64 : L;
 }
 
-// library streams and events of one device, created on first use; a call
-// holds the device's lock while it enqueues, so calls from several host
-// threads do not interleave on them
-struct DeviceQueues {
-    std::mutex mu;
-    cudaStream_t pro = nullptr, pre = nullptr;
-    cudaEvent_t start = nullptr, end = nullptr, pro_done[2] = {}, pre_done[2] = {};
-    bool ready = false;
-};
-
-DeviceQueues g_queues[64];
-
-// with q.mu held
-cudaError_t queues_ready(DeviceQueues &q) {
-    if (!q.ready) {
-        int lo = 0, hi = 0;
-        cudaError_t e = cudaDeviceGetStreamPriorityRange(&lo, &hi);
-        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&q.pro, cudaStreamNonBlocking, lo);
-        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&q.pre, cudaStreamNonBlocking, hi);
-        cudaEvent_t *evs[6] = {&q.start, &q.end, &q.pro_done[0], &q.pro_done[1], &q.pre_done[0],
-                               &q.pre_done[1]};
-        for (int i = 0; i < 6 && e == cudaSuccess; ++i)
-            e = cudaEventCreateWithFlags(evs[i], cudaEventDisableTiming);
-        if (e != cudaSuccess) return e;
-        q.ready = true;
+// the call's events, destroyed when the call returns
+struct CallEvents {
+    cudaEvent_t ev[5] = {};   // start, pro_done[2], pre_done[2]
+    cudaError_t create() {
+        for (auto &e : ev) {
+            const cudaError_t r = cudaEventCreateWithFlags(&e, cudaEventDisableTiming);
+            if (r != cudaSuccess) return r;
+        }
+        return cudaSuccess;
     }
-    return cudaSuccess;
-}
+    ~CallEvents() {
+        for (auto e : ev)
+            if (e != nullptr) cudaEventDestroy(e);
+    }
+};
 
 }  // namespace
 
@@ -85,7 +75,7 @@ cudaError_t launch_prologue_prefill(const void *q_raw, const void *k_raw, const 
                                     const float *init_state, int64_t T, int32_t H, int32_t D,
                                     kda_dtype dt, int64_t segment_tokens, void *out,
                                     float *final_state, void *workspace, bool use_chunk,
-                                    cudaStream_t user) {
+                                    cudaStream_t user, cudaStream_t pro) {
     const int64_t L = seg_tokens_of(T, segment_tokens);
     const Ring R = ring_layout(H, D, dt, L);
     uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -95,21 +85,17 @@ cudaError_t launch_prologue_prefill(const void *q_raw, const void *k_raw, const 
     const size_t sbytes = static_cast<size_t>(H) * D * D * sizeof(float);
     const size_t esz = dt == KDA_BF16 ? 2 : 4;
 
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    CallEvents E;
+    cudaError_t e = E.create();
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    DeviceQueues *Q = &g_queues[dev];
-    std::lock_guard<std::mutex> lock(Q->mu);
-    if ((e = queues_ready(*Q)) != cudaSuccess) return e;
+    cudaEvent_t start = E.ev[0], pro_done[2] = {E.ev[1], E.ev[2]}, pre_done[2] = {E.ev[3], E.ev[4]};
 
     if ((e = cudaMemsetAsync(status, 0, 4, user)) != cudaSuccess) return e;
     e = init_state ? cudaMemcpyAsync(state, init_state, sbytes, cudaMemcpyDeviceToDevice, user)
                    : cudaMemsetAsync(state, 0, sbytes, user);
     if (e != cudaSuccess) return e;
-    if ((e = cudaEventRecord(Q->start, user)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(Q->pro, Q->start, 0)) != cudaSuccess) return e;
-    if ((e = cudaStreamWaitEvent(Q->pre, Q->start, 0)) != cudaSuccess) return e;
+    if ((e = cudaEventRecord(start, user)) != cudaSuccess) return e;
+    if ((e = cudaStreamWaitEvent(pro, start, 0)) != cudaSuccess) return e;
 
     const int64_t nseg = (T + L - 1) / L;
     for (int64_t s = 0; s < nseg; ++s) {
@@ -117,29 +103,28 @@ cudaError_t launch_prologue_prefill(const void *q_raw, const void *k_raw, const 
         const int64_t tb = s * L, te = tb + L < T ? tb + L : T;
         uint8_t *r = ring[b];
         // the prologue of segment s into buffer b, once segment s - 2's prefill has read it
-        if (s >= 2 && (e = cudaStreamWaitEvent(Q->pro, Q->pre_done[b], 0)) != cudaSuccess) return e;
+        if (s >= 2 && (e = cudaStreamWaitEvent(pro, pre_done[b], 0)) != cudaSuccess) return e;
         e = launch_prologue_range(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, nullptr, 1, T, tb, te, H, D,
                                   dt, r + R.q, r + R.k, r + R.v, reinterpret_cast<float *>(r + R.g),
-                                  reinterpret_cast<float *>(r + R.beta), Q->pro);
+                                  reinterpret_cast<float *>(r + R.beta), pro);
         if (e != cudaSuccess) return e;
-        if ((e = cudaEventRecord(Q->pro_done[b], Q->pro)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(pro_done[b], pro)) != cudaSuccess) return e;
         // its prefill, continuing the state
-        if ((e = cudaStreamWaitEvent(Q->pre, Q->pro_done[b], 0)) != cudaSuccess) return e;
+        if ((e = cudaStreamWaitEvent(user, pro_done[b], 0)) != cudaSuccess) return e;
         void *o = static_cast<uint8_t *>(out) + static_cast<size_t>(tb) * H * D * esz;
         const float *gp = reinterpret_cast<const float *>(r + R.g);
         const float *bp = reinterpret_cast<const float *>(r + R.beta);
         e = use_chunk ? launch_prefill_chunk(r + R.q, r + R.k, r + R.v, gp, bp, state, nullptr, 1, te - tb,
-                                             H, o, state, status, Q->pre)
+                                             H, o, state, status, user)
                       : launch_prefill_recurrent(r + R.q, r + R.k, r + R.v, gp, bp, state, nullptr, 1,
-                                                 te - tb, H, D, dt, o, state, status, Q->pre);
+                                                 te - tb, H, D, dt, o, state, status, user);
         if (e != cudaSuccess) return e;
-        if ((e = cudaEventRecord(Q->pre_done[b], Q->pre)) != cudaSuccess) return e;
+        if ((e = cudaEventRecord(pre_done[b], user)) != cudaSuccess) return e;
     }
     if (final_state != nullptr &&
-        (e = cudaMemcpyAsync(final_state, state, sbytes, cudaMemcpyDeviceToDevice, Q->pre)) != cudaSuccess)
+        (e = cudaMemcpyAsync(final_state, state, sbytes, cudaMemcpyDeviceToDevice, user)) != cudaSuccess)
         return e;
-    if ((e = cudaEventRecord(Q->end, Q->pre)) != cudaSuccess) return e;
-    return cudaStreamWaitEvent(user, Q->end, 0);
+    return cudaSuccess;
 }
 
 }  // namespace kda

@@ -50,7 +50,7 @@ lib.kda_prefill_segmented.argtypes = [_P, _P, _P, _P, _P, _P, _i64, kda_dims, _i
 lib.kda_prologue_prefill_workspace_size.argtypes = [kda_dims, _i64, _i64]
 lib.kda_prologue_prefill_workspace_size.restype = _sz
 lib.kda_prologue_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i64, kda_dims, _i64, _P, _P, _P,
-                                     _sz, _P]
+                                     _sz, _P, _P]
 lib.kda_decode_step.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, kda_dims, _P]
 lib.kda_prologue.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
                              _P, _P, _P]
@@ -207,11 +207,26 @@ def kda_prologue_prefill_workspace_size(H: int, d: int, dtype: torch.dtype, T: i
     return int(lib.kda_prologue_prefill_workspace_size(kda_dims(H, d, d, code), T, segment_tokens))
 
 
+_side_streams = {}
+
+
+def _side_stream(dev):
+    """This binding's stream for the prologues (one per device, lowest priority)."""
+    key = torch.device(dev).index if torch.device(dev).index is not None else torch.cuda.current_device()
+    if key not in _side_streams:
+        _side_streams[key] = torch.cuda.Stream(device=key, priority=0)
+    return _side_streams[key]
+
+
 def kda_prologue_prefill(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, init_state=None,
-                         segment_tokens=16384, out=None, final_state=None, workspace=None):
+                         segment_tokens=16384, out=None, final_state=None, workspace=None,
+                         prologue_stream=None):
     """Prologue + prefill of one document from raw projections, segment by
     segment with the next prologue overlapping the current prefill; returns
-    (out, final_state [H, d, d])."""
+    (out, final_state [H, d, d]).  The prefills run on the current stream, the
+    prologues on `prologue_stream` (a torch.cuda.Stream; by default one that
+    this module keeps per device, at the lowest priority: run the call on a
+    higher-priority current stream for the best overlap)."""
     T, H, d = q_raw.shape
     dev = q_raw.device
     _dev(q_raw, "q_raw")
@@ -232,9 +247,11 @@ def kda_prologue_prefill(q_raw, k_raw, v_raw, conv_w, z_g, z_beta, init_state=No
     if workspace is None:
         workspace = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     _dev(workspace, "workspace", torch.uint8)
+    side = prologue_stream if prologue_stream is not None else _side_stream(dev)
     st = lib.kda_prologue_prefill(_ptr(q_raw), _ptr(k_raw), _ptr(v_raw), _ptr(conv_w), _ptr(z_g),
                                   _ptr(z_beta), _ptr(init_state), T, dims, segment_tokens, _ptr(out),
-                                  _ptr(final_state), _ptr(workspace), workspace.numel(), _stream())
+                                  _ptr(final_state), _ptr(workspace), workspace.numel(), _stream(),
+                                  ctypes.c_void_p(side.cuda_stream))
     if st != KDA_OK:
         raise KDAError(st, "kda_prologue_prefill")
     return out, final_state

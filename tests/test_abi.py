@@ -96,7 +96,7 @@ def test_segmented_prefill_argument_checks(kda):
     assert kda.lib.kda_prefill_segmented_workspace_size(d, 4096, 0) == 0
     call = lambda **o: kda.lib.kda_prefill_segmented(
         o.get("q", p), p, p, p, p, None, o.get("T", 4096), d, o.get("nseg", 4), p, None,
-        o.get("ws", p), o.get("wsb", ws), None)
+        o.get("ws", p), o.get("wsb", ws), None, None)
     assert call(nseg=0) == kda.KDA_ERR_INVALID and "num_segments" in kda.kda_last_error()
     assert call(q=None) == kda.KDA_ERR_INVALID
     assert call(ws=ctypes.c_void_p(FAKE + 16)) == kda.KDA_ERR_INVALID   # 256-byte alignment
@@ -112,7 +112,7 @@ def test_prologue_prefill_argument_checks(kda):
     assert kda.lib.kda_prologue_prefill_workspace_size(d, 4096, 0) == 0
     call = lambda **o: kda.lib.kda_prologue_prefill(
         p, p, p, p, o.get("zg", p), p, None, o.get("T", 4096), d, o.get("seg", 1024), p, None,
-        o.get("ws", p), o.get("wsb", ws), None)
+        o.get("ws", p), o.get("wsb", ws), None, None)
     assert call(seg=0) == kda.KDA_ERR_INVALID and "segment_tokens" in kda.kda_last_error()
     assert call(zg=None) == kda.KDA_ERR_INVALID and "z_g" in kda.kda_last_error()
     assert call(ws=ctypes.c_void_p(FAKE + 16)) == kda.KDA_ERR_INVALID
