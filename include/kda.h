@@ -78,6 +78,11 @@ typedef enum { KDA_F32 = 0, KDA_BF16 = 1 } kda_dtype;
 #define KDA_DEVICE_RANGE 3        /* a value the tensor-core prefill keeps in fp16 operands (v, the
                                      state, the pseudo-values) reached 65504 in magnitude: the
                                      results of that call are not valid                          */
+#define KDA_DEVICE_BAD_SNAPSHOT 4 /* a snapshot offset outside (0, T], out of order, or neither a
+                                     multiple of KDA_SNAPSHOT_ALIGN into its document nor its end */
+
+/* Prefix snapshots are taken every multiple of this many tokens into a document. */
+#define KDA_SNAPSHOT_ALIGN 64
 
 typedef struct {
     int32_t H;          /* heads                                   */
@@ -125,6 +130,37 @@ KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v,
                        int32_t N, int64_t T, kda_dims dims, void *out,
                        float *final_state, void *workspace,
                        size_t workspace_bytes, void *stream);
+
+/*
+ * kda_prefill that also keeps prefix snapshots: the state at given token
+ * boundaries, so that a later request sharing that prefix can resume from it
+ * ("From GPT-2 to Kimi K3, from first principles", Chapter 14: KDA states
+ * stored sparsely at fixed token boundaries and restored to resume prefill).
+ * Arguments and results as kda_prefill, plus:
+ *   snapshot_offsets [n_snapshots] int32 device, strictly increasing token
+ *              offsets into the packed T tokens.  Offset p names the
+ *              document with bos < p <= eos (its cu_seqlens bounds) and the
+ *              state after that document's tokens [bos, p): each p must be a
+ *              multiple of KDA_SNAPSHOT_ALIGN (64) tokens into its document,
+ *              or that document's end.
+ *   n_snapshots  >= 0; 0 makes the call kda_prefill
+ *   snapshots  [n_snapshots, H, d_k, d_v] fp32 device, written (state i in
+ *              final_state's layout); caller-owned
+ * Resuming: kda_prefill of the document's tokens [p, eos) with init_state =
+ * snapshots[i] gives the same outputs and final state as the full run, up
+ * to rounding.  Offsets that break the rules set KDA_DEVICE_BAD_SNAPSHOT in
+ * the workspace's status word (read it with kda_get_device_status); the
+ * snapshots are then unspecified, the outputs and final states are not
+ * affected.  Errors as kda_prefill, and KDA_ERR_INVALID for n_snapshots < 0
+ * or a missing snapshot_offsets / snapshots pointer.
+ */
+KDA_API kda_status kda_prefill_snapshots(const void *q, const void *k, const void *v,
+                                         const float *g, const float *beta,
+                                         const float *init_state, const int32_t *cu_seqlens,
+                                         int32_t N, int64_t T, kda_dims dims, void *out,
+                                         float *final_state, const int32_t *snapshot_offsets,
+                                         int32_t n_snapshots, float *snapshots, void *workspace,
+                                         size_t workspace_bytes, void *stream);
 
 /*
  * Bytes of device workspace kda_prologue_prefill needs (0 for invalid

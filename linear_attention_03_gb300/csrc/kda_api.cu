@@ -95,13 +95,13 @@ size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N) {
     return kStatusBytes + kda::doc_order_bytes(N);
 }
 
-kda_status kda_prefill(const void *q, const void *k, const void *v,
-                       const float *g, const float *beta,
-                       const float *init_state, const int32_t *cu_seqlens,
-                       int32_t N, int64_t T, kda_dims dims, void *out,
-                       float *final_state, void *workspace,
-                       size_t workspace_bytes, void *stream) {
-    g_last_error[0] = '\0';
+namespace {
+
+kda_status prefill_impl(const void *q, const void *k, const void *v, const float *g,
+                        const float *beta, const float *init_state, const int32_t *cu_seqlens,
+                        int32_t N, int64_t T, kda_dims dims, void *out, float *final_state,
+                        kda::Snapshots snaps, void *workspace, size_t workspace_bytes,
+                        void *stream) {
     KDA_TRY(check_dims(dims));
     if (N < 1 || N > 65535) return fail(KDA_ERR_INVALID, "N must be in [1, 65535]%s");
     if (T < 0 || T > INT32_MAX) return fail(KDA_ERR_INVALID, "T must be in [0, 2^31)%s");
@@ -135,16 +135,54 @@ kda_status kda_prefill(const void *q, const void *k, const void *v,
         if (err != cudaSuccess) return cuda_fail(err, "document order launch");
         order = ord;
     }
+    if (snaps.n > 0) {
+        err = kda::launch_snapshot_check(snaps.offsets, snaps.n, cu_seqlens, N, T, status, s);
+        if (err != cudaSuccess) return cuda_fail(err, "snapshot offset check launch");
+    }
     const kda_dtype dt = (kda_dtype)dims.qkv_dtype;
     if (T > 0 && kda::chunk_prefill_supported(dims.d_k, dt) && !force_recurrent())
         err = kda::launch_prefill_chunk(q, k, v, g, beta, init_state, cu_seqlens, N, T, dims.H,
-                                        out, final_state, status, s, order);
+                                        out, final_state, status, s, order, nullptr, snaps);
     else
         err = kda::launch_prefill_recurrent(q, k, v, g, beta, init_state, cu_seqlens, N, T,
                                             dims.H, dims.d_k, dt, out, final_state, status, s,
-                                            order);
+                                            order, snaps);
     if (err != cudaSuccess) return cuda_fail(err, "prefill launch");
     return KDA_OK;
+}
+
+}  // namespace
+
+kda_status kda_prefill(const void *q, const void *k, const void *v,
+                       const float *g, const float *beta,
+                       const float *init_state, const int32_t *cu_seqlens,
+                       int32_t N, int64_t T, kda_dims dims, void *out,
+                       float *final_state, void *workspace,
+                       size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    return prefill_impl(q, k, v, g, beta, init_state, cu_seqlens, N, T, dims, out, final_state, {},
+                        workspace, workspace_bytes, stream);
+}
+
+kda_status kda_prefill_snapshots(const void *q, const void *k, const void *v,
+                                 const float *g, const float *beta,
+                                 const float *init_state, const int32_t *cu_seqlens,
+                                 int32_t N, int64_t T, kda_dims dims, void *out,
+                                 float *final_state, const int32_t *snapshot_offsets,
+                                 int32_t n_snapshots, float *snapshots, void *workspace,
+                                 size_t workspace_bytes, void *stream) {
+    g_last_error[0] = '\0';
+    if (n_snapshots < 0) return fail(KDA_ERR_INVALID, "n_snapshots must be >= 0%s");
+    if (n_snapshots > 0) {
+        KDA_TRY(need4(snapshot_offsets, "snapshot_offsets"));
+        KDA_TRY(need(snapshots, "snapshots"));
+    }
+    kda::Snapshots snaps;
+    snaps.offsets = n_snapshots > 0 ? snapshot_offsets : nullptr;
+    snaps.n = n_snapshots;
+    snaps.out = n_snapshots > 0 ? snapshots : nullptr;
+    return prefill_impl(q, k, v, g, beta, init_state, cu_seqlens, N, T, dims, out, final_state, snaps,
+                        workspace, workspace_bytes, stream);
 }
 
 size_t kda_prologue_prefill_workspace_size(kda_dims dims, int64_t T, int64_t segment_tokens) {
@@ -402,6 +440,8 @@ kda_status kda_get_device_status(const void *workspace, int32_t *status_out,
         return fail(KDA_ERR_TIMEOUT, "a device-side wait gave up%s");
     if (word == KDA_DEVICE_RANGE)
         return fail(KDA_ERR_DEVICE, "a value held in fp16 operands reached 65504 in magnitude%s");
+    if (word == KDA_DEVICE_BAD_SNAPSHOT)
+        return fail(KDA_ERR_DEVICE, "a snapshot offset is out of range, out of order or misaligned%s");
     return fail(KDA_ERR_DEVICE, "the device rejected cu_seqlens (not 0..T, non-decreasing)%s");
 }
 

@@ -80,6 +80,28 @@ __device__ __forceinline__ void flag_status(int32_t *status, int32_t code) {
     if (status != nullptr) atomicCAS(status, KDA_DEVICE_OK, code);
 }
 
+// Prefix snapshots ("From GPT-2 to Kimi K3, from first principles", Chapter 14:
+// the state kept at fixed token boundaries so that a later request with the
+// same prefix resumes from it).  offsets[i] (strictly increasing, in the packed
+// token axis) names the state of the document with bos < offsets[i] <= eos
+// after its tokens [bos, offsets[i]); it goes to out[i] ([H, d_k, d_v] fp32,
+// laid out as final_state).  A kernel writes the entries of its own document.
+struct Snapshots {
+    const int32_t *offsets = nullptr;
+    int32_t n = 0;
+    float *out = nullptr;
+};
+
+// the first snapshot index whose offset lies past bos (n when none)
+__device__ __forceinline__ int32_t snap_first(const Snapshots &s, int64_t bos) {
+    int32_t lo = 0, hi = s.n;
+    while (lo < hi) {
+        const int32_t mid = (lo + hi) >> 1;
+        if (static_cast<int64_t>(s.offsets[mid]) <= bos) lo = mid + 1; else hi = mid;
+    }
+    return lo;
+}
+
 // Count of kernels queued by this library (kda_kernel_launches).
 void count_launches(uint64_t n);
 
@@ -131,7 +153,14 @@ cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      int64_t T, int32_t H, int32_t D,
                                      kda_dtype dt, void *out,
                                      float *final_state, int32_t *status,
-                                     cudaStream_t stream, const int32_t *order = nullptr);
+                                     cudaStream_t stream, const int32_t *order = nullptr,
+                                     Snapshots snaps = {});
+
+// checks snapshot offsets (in (0, T], strictly increasing, each a multiple of
+// KDA_SNAPSHOT_ALIGN tokens into its document or that document's end) and sets
+// KDA_DEVICE_BAD_SNAPSHOT in the status word when one is not
+cudaError_t launch_snapshot_check(const int32_t *offsets, int32_t n, const int32_t *cu_seqlens,
+                                  int32_t N, int64_t T, int32_t *status, cudaStream_t stream);
 
 // the documents of a packed batch, longest first (chunk count, decreasing):
 // order[i] is the document whose CTAs take grid row i.  doc_order_bytes(N) is
@@ -163,7 +192,7 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
                                  void *out, float *final_state, int32_t *status,
                                  cudaStream_t stream, const int32_t *order = nullptr,
-                                 float *out_f32 = nullptr);
+                                 float *out_f32 = nullptr, Snapshots snaps = {});
 
 // prologue and prefill of one document, segment by segment, overlapped
 size_t pipeline_workspace_size(int32_t H, int32_t D, kda_dtype dt, int64_t T, int64_t segment_tokens);

@@ -13,7 +13,9 @@
 //     u_j = beta (v_j - a_j),  o_j = b_j + u_j (k . q),
 //     S_ij <- alpha_i S_ij + k_i u_j.
 // Token inputs are staged through shared memory TT tokens at a time; every
-// thread then reads the same address (broadcast).
+// thread then reads the same address (broadcast).  Prefix snapshots are
+// written from the registers at stage boundaries (every snapshot offset is
+// a multiple of 64 tokens into its document, or its end).
 #include "kda_internal.cuh"
 
 namespace kda {
@@ -28,7 +30,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
                  const float *__restrict__ beta, const float *init_state,
                  const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
                  Tin *__restrict__ out, float *final_state,
-                 int32_t *__restrict__ status, const int32_t *__restrict__ order) {
+                 int32_t *__restrict__ status, const int32_t *__restrict__ order, Snapshots snaps) {
     constexpr int NW = (D + 31) / 32;
     constexpr int LANES = D < 32 ? D : 32;           // lanes of a (partial) warp
     constexpr unsigned MASK = D < 32 ? ((1u << D) - 1u) : 0xffffffffu;
@@ -54,9 +56,20 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
 #pragma unroll
     for (int i = 0; i < D; ++i)
         S[i] = init_state ? init_state[unit * D * D + (size_t)i * D + j] : 0.f;
+    // the document's next snapshot: its state after the tokens before offsets[snap]
+    int32_t snap = snaps.n > 0 ? snap_first(snaps, bos) : 0;
+    auto take_snapshot = [&](int64_t at) {
+        if (snap < snaps.n && static_cast<int64_t>(snaps.offsets[snap]) == at) {
+            float *dst = snaps.out + ((size_t)snap * H + h) * D * D + j;
+#pragma unroll
+            for (int i = 0; i < D; ++i) dst[(size_t)i * D] = S[i];
+            ++snap;
+        }
+    };
 
     for (int64_t t0 = bos; t0 < eos; t0 += kStage) {
         const int cnt = (int)((eos - t0) < kStage ? (eos - t0) : kStage);
+        if (t0 > bos) take_snapshot(t0);
         __syncthreads();
         for (int tt = 0; tt < cnt; ++tt) {
             const size_t row = (size_t)(t0 + tt) * H + h;
@@ -103,6 +116,7 @@ recurrent_kernel(const Tin *__restrict__ q, const Tin *__restrict__ k,
             }
         }
     }
+    if (eos > bos) take_snapshot(eos);
     if (final_state) {
 #pragma unroll
         for (int i = 0; i < D; ++i) final_state[unit * D * D + (size_t)i * D + j] = S[i];
@@ -113,11 +127,11 @@ template <typename Tin, int D>
 cudaError_t run(const void *q, const void *k, const void *v, const float *g,
                 const float *beta, const float *init_state, const int32_t *cu,
                 int32_t N, int64_t T, int32_t H, void *out, float *final_state,
-                int32_t *status, cudaStream_t stream, const int32_t *order) {
+                int32_t *status, cudaStream_t stream, const int32_t *order, Snapshots snaps) {
     recurrent_kernel<Tin, D><<<dim3(H, N), D, 0, stream>>>(
         static_cast<const Tin *>(q), static_cast<const Tin *>(k),
         static_cast<const Tin *>(v), g, beta, init_state, cu, N, T, H,
-        static_cast<Tin *>(out), final_state, status, order);
+        static_cast<Tin *>(out), final_state, status, order, snaps);
     count_launches(1);
     return cudaGetLastError();
 }
@@ -126,12 +140,13 @@ template <typename Tin>
 cudaError_t run_d(const void *q, const void *k, const void *v, const float *g,
                   const float *beta, const float *init_state, const int32_t *cu,
                   int32_t N, int64_t T, int32_t H, int32_t D, void *out,
-                  float *final_state, int32_t *status, cudaStream_t stream, const int32_t *order) {
+                  float *final_state, int32_t *status, cudaStream_t stream, const int32_t *order,
+                  Snapshots snaps) {
     switch (D) {
-    case 16: return run<Tin, 16>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
-    case 32: return run<Tin, 32>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
-    case 64: return run<Tin, 64>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
-    case 128: return run<Tin, 128>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order);
+    case 16: return run<Tin, 16>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order, snaps);
+    case 32: return run<Tin, 32>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order, snaps);
+    case 64: return run<Tin, 64>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order, snaps);
+    case 128: return run<Tin, 128>(q, k, v, g, beta, init_state, cu, N, T, H, out, final_state, status, stream, order, snaps);
     default: return cudaErrorInvalidValue;
     }
 }
@@ -145,12 +160,54 @@ cudaError_t launch_prefill_recurrent(const void *q, const void *k,
                                      int64_t T, int32_t H, int32_t D,
                                      kda_dtype dt, void *out,
                                      float *final_state, int32_t *status,
-                                     cudaStream_t stream, const int32_t *order) {
+                                     cudaStream_t stream, const int32_t *order, Snapshots snaps) {
     if (dt == KDA_BF16)
         return run_d<__nv_bfloat16>(q, k, v, g, beta, init_state, cu_seqlens, N, T, H, D,
-                                    out, final_state, status, stream, order);
+                                    out, final_state, status, stream, order, snaps);
     return run_d<float>(q, k, v, g, beta, init_state, cu_seqlens, N, T, H, D, out,
-                        final_state, status, stream, order);
+                        final_state, status, stream, order, snaps);
+}
+
+namespace {
+
+// one thread per offset: in (0, T], above its predecessor, and a multiple of
+// KDA_SNAPSHOT_ALIGN into the document with bos < p <= eos, or that eos
+__global__ void snapshot_check_kernel(const int32_t *__restrict__ offsets, int32_t n,
+                                      const int32_t *__restrict__ cu, int32_t N, int64_t T,
+                                      int32_t *__restrict__ status) {
+    const int32_t i = blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int64_t p = offsets[i];
+    bool ok = p > 0 && p <= T && (i == 0 || static_cast<int64_t>(offsets[i - 1]) < p);
+    if (ok) {
+        int64_t bos = 0, eos = T;
+        if (cu != nullptr) {
+            // the first document end at or past p: its document holds p
+            int32_t lo = 0, hi = N;
+            while (lo < hi) {
+                const int32_t mid = (lo + hi) >> 1;
+                if (static_cast<int64_t>(cu[mid + 1]) < p) lo = mid + 1; else hi = mid;
+            }
+            if (lo >= N) {
+                ok = false;
+            } else {
+                bos = cu[lo];
+                eos = cu[lo + 1];
+            }
+        }
+        ok = ok && bos < p && p <= eos && ((p - bos) % KDA_SNAPSHOT_ALIGN == 0 || p == eos);
+    }
+    if (!ok) flag_status(status, KDA_DEVICE_BAD_SNAPSHOT);
+}
+
+}  // namespace
+
+cudaError_t launch_snapshot_check(const int32_t *offsets, int32_t n, const int32_t *cu_seqlens,
+                                  int32_t N, int64_t T, int32_t *status, cudaStream_t stream) {
+    if (n <= 0) return cudaSuccess;
+    snapshot_check_kernel<<<(n + 255) / 256, 256, 0, stream>>>(offsets, n, cu_seqlens, N, T, status);
+    count_launches(1);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

@@ -24,13 +24,16 @@ lib = ctypes.CDLL(_LIB_PATH)
 KDA_OK, KDA_ERR_INVALID, KDA_ERR_UNSUPPORTED, KDA_ERR_CUDA, KDA_ERR_TIMEOUT, \
     KDA_ERR_DEVICE = range(6)
 KDA_F32, KDA_BF16 = 0, 1
-KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT, KDA_DEVICE_RANGE = 0, 1, 2, 3
+KDA_DEVICE_OK, KDA_DEVICE_BAD_OFFSETS, KDA_DEVICE_TIMEOUT, KDA_DEVICE_RANGE, \
+    KDA_DEVICE_BAD_SNAPSHOT = range(5)
+KDA_SNAPSHOT_ALIGN = 64
 SYMBOLS = ("kda_prefill_workspace_size", "kda_prefill", "kda_decode_step",
            "kda_prologue", "kda_get_device_status", "kda_last_error",
            "kda_kernel_launches", "kda_decode_step_conv", "kda_decode_verify",
            "kda_output_gate", "kda_prefill_noalloc", "kda_selftest_wait",
            "kda_prefill_segmented_workspace_size", "kda_prefill_segmented",
-           "kda_prologue_prefill_workspace_size", "kda_prologue_prefill")
+           "kda_prologue_prefill_workspace_size", "kda_prologue_prefill",
+           "kda_prefill_snapshots")
 
 
 class kda_dims(ctypes.Structure):
@@ -43,6 +46,8 @@ lib.kda_prefill_workspace_size.argtypes = [kda_dims, _i64, _i32]
 lib.kda_prefill_workspace_size.restype = _sz
 lib.kda_prefill.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P, _P,
                             _sz, _P]
+lib.kda_prefill_snapshots.argtypes = [_P, _P, _P, _P, _P, _P, _P, _i32, _i64, kda_dims, _P, _P,
+                                      _P, _i32, _P, _P, _sz, _P]
 lib.kda_prefill_segmented_workspace_size.argtypes = [kda_dims, _i64, _i32]
 lib.kda_prefill_segmented_workspace_size.restype = _sz
 lib.kda_prefill_segmented.argtypes = [_P, _P, _P, _P, _P, _P, _i64, kda_dims, _i32, _P, _P, _P,
@@ -64,7 +69,8 @@ lib.kda_last_error.argtypes = []
 lib.kda_last_error.restype = ctypes.c_char_p
 lib.kda_kernel_launches.argtypes = []
 lib.kda_kernel_launches.restype = ctypes.c_uint64
-for _fn in (lib.kda_prefill, lib.kda_prefill_segmented, lib.kda_prologue_prefill,
+for _fn in (lib.kda_prefill, lib.kda_prefill_snapshots, lib.kda_prefill_segmented,
+            lib.kda_prologue_prefill,
             lib.kda_decode_step, lib.kda_prologue,
             lib.kda_get_device_status,
             lib.kda_decode_step_conv, lib.kda_decode_verify, lib.kda_output_gate):
@@ -136,6 +142,23 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     bytes (the status word, then the documents' longest-first order when
     there are several); 256 bytes also work and run the documents in order.
     """
+    out, final_state, _ = _prefill(q, k, v, g, beta, init_state, cu_seqlens, out, final_state,
+                                   workspace, want_final_state, None, None)
+    return out, final_state
+
+
+def kda_prefill_snapshots(q, k, v, g, beta, snapshot_offsets, init_state=None, cu_seqlens=None,
+                          out=None, final_state=None, snapshots=None, workspace=None):
+    """kda_prefill that also returns the states at `snapshot_offsets` (int32
+    device tensor of strictly increasing packed-token offsets, each a multiple
+    of KDA_SNAPSHOT_ALIGN tokens into its document or its end); returns
+    (out, final_state, snapshots [n, H, d, d] fp32)."""
+    return _prefill(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, workspace, True,
+                    snapshot_offsets, snapshots)
+
+
+def _prefill(q, k, v, g, beta, init_state, cu_seqlens, out, final_state, workspace,
+             want_final_state, snapshot_offsets, snapshots):
     T, H, d = q.shape
     dev = q.device
     _dev(q, "q")
@@ -156,12 +179,25 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     if workspace is None:
         workspace = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     _dev(workspace, "workspace", torch.uint8)
-    st = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
-                         _ptr(cu), N, T, dims, _ptr(out), _ptr(final_state),
-                         _ptr(workspace), workspace.numel(), _stream())
+    if snapshot_offsets is None:
+        st = lib.kda_prefill(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                             _ptr(cu), N, T, dims, _ptr(out), _ptr(final_state),
+                             _ptr(workspace), workspace.numel(), _stream())
+        if st != KDA_OK:
+            raise KDAError(st, "kda_prefill")
+        return out, final_state, None
+    _dev(snapshot_offsets, "snapshot_offsets", torch.int32)
+    n_snap = snapshot_offsets.numel()
+    if snapshots is None:
+        snapshots = torch.empty((n_snap, H, d, d), dtype=torch.float32, device=dev)
+    _dev(snapshots, "snapshots", torch.float32, (n_snap, H, d, d))
+    st = lib.kda_prefill_snapshots(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta),
+                                   _ptr(init_state), _ptr(cu), N, T, dims, _ptr(out),
+                                   _ptr(final_state), _ptr(snapshot_offsets), n_snap,
+                                   _ptr(snapshots), _ptr(workspace), workspace.numel(), _stream())
     if st != KDA_OK:
-        raise KDAError(st, "kda_prefill")
-    return out, final_state
+        raise KDAError(st, "kda_prefill_snapshots")
+    return out, final_state, snapshots
 
 
 def kda_prefill_segmented_workspace_size(H: int, d: int, dtype: torch.dtype, T: int,

@@ -172,3 +172,15 @@ def test_decode_with_conv_cache_argument_checks(kda):
     assert call(N=0) == kda.KDA_OK
     assert call(cache=None) == kda.KDA_ERR_INVALID and "conv_state" in kda.kda_last_error()
     assert call(state=None) == kda.KDA_ERR_INVALID and "state" in kda.kda_last_error()
+
+
+def test_prefill_snapshots_argument_checks(kda):
+    p = ctypes.c_void_p(FAKE)
+    d = dims(kda)
+    call = lambda **o: kda.lib.kda_prefill_snapshots(
+        p, p, p, p, p, None, None, 1, 256, d, p, None, o.get("offs", p), o.get("n", 2),
+        o.get("snaps", p), p, 256, None)
+    assert call(n=-1) == kda.KDA_ERR_INVALID and "n_snapshots" in kda.kda_last_error()
+    assert call(offs=None) == kda.KDA_ERR_INVALID and "snapshot_offsets" in kda.kda_last_error()
+    assert call(snaps=None) == kda.KDA_ERR_INVALID and "snapshots" in kda.kda_last_error()
+    assert call(snaps=ctypes.c_void_p(FAKE + 4)) == kda.KDA_ERR_INVALID   # 16-byte alignment
