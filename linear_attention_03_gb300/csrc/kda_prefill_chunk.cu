@@ -49,6 +49,9 @@
 //   warps 0..3   the state chain of chunk x: the state's fp16 copy, -(K+ S)
 //                and Q+ S, Tb V + Tb (-K+ S), S += Khat^T U and O += P U, the
 //                outputs of chunk x - 1 out under chunk x's first MMA
+// Prefix snapshots (every offset 64 tokens into a document, or its end) are
+// written by the chain warps from the state's fp32 TMEM copy as they read it
+// at the top of a chunk, and at the end.
 // All waits are bounded: a lost arrival sets KDA_DEVICE_TIMEOUT, every later
 // wait of the CTA returns at once, and the CTA leaves after draining its own
 // outstanding copies and MMAs.
@@ -95,7 +98,7 @@ constexpr uint32_t OFF_X = 220288, XS = 20;
 // e^{G_31} per channel, three slots; beta of a chunk, two slots
 constexpr uint32_t OFF_VEC = 221568, VEC_D = 0, VEC_BETA = 1536;
 // mbarriers.  Loads: BAR_QK[2], BAR_V[3] (transaction bytes).  MMA completion
-// (tcgen05.commit): BAR_G, BAR_1, BAR_2, BAR_3, and the slot releases EMPTY_B[3]
+// (tcgen05.commit): BAR_G, BAR_1, BAR_2, BAR_3 (the state), BAR_O (the outputs), and the slot releases EMPTY_B[3]
 // (MMA3 of the chunk done: its -K+/Q+/Khat slot), TB_FREE[2], PM_FREE[2].
 // Hand-overs: FULL_B[3] (8 pass warps stored a chunk's operands), TB_FULL[2]
 // (Tb complete and v converted: 2 warps), TG_FREE (3 readout warps read the
@@ -104,7 +107,7 @@ constexpr uint32_t OFF_BAR = OFF_VEC + 2048;
 constexpr uint32_t BAR_QK = 0, BAR_V = 16, BAR_G = 40, BAR_1 = 48, BAR_2 = 56, BAR_3 = 64,
                    FULL_B = 72, EMPTY_B = 96, TB_FULL = 120, TB_FREE = 136, PM_FREE = 152,
                    TG_FREE = 168, BAR_DR0 = 176, BAR_DR1 = 184, T_READY = 192, L_FREE = 208,
-                   NUM_BARS = 28;
+                   BAR_O = 224, NUM_BARS = 29;
 // tmem base, abort flag, then the last chunk whose load went to each q/k and v slot
 constexpr uint32_t OFF_MISC = OFF_BAR + 8 * NUM_BARS;
 constexpr uint32_t MISC_TMEM = 0, MISC_ABORT = 1, MISC_QK = 2, MISC_V = 4;
@@ -119,6 +122,7 @@ constexpr uint32_t TM_U = 320;    // U^T fp32, 32 columns
 constexpr uint32_t TM_XB = 352;   // -(K+ S)^T fp16 (A operand, K = 32)
 constexpr uint32_t TM_UB = 368;   // U^T fp16 (A operand, K = 32)
 constexpr uint32_t TM_G = 384;    // Gram, 80 columns
+constexpr uint32_t TM_UL = 464;   // U^T - fp16(U^T), fp16 (the low half of U for O += P U)
 constexpr uint32_t TM_COLS = 512;
 
 // ---- the map checked at compile time ----
@@ -139,10 +143,10 @@ static_assert(L_BUF >= kC * LST * 4 && OFF_L + 2 * L_BUF <= OFF_LO && OFF_LO + k
               "L, lo partials");
 static_assert(OFF_X + 16 * XS * 4 <= OFF_VEC && VEC_BETA >= 3 * kD * 4 && VEC_BETA + 2 * kC * 4 <= 2048,
               "scratch, vectors");
-static_assert(L_FREE + 16 <= 8 * NUM_BARS, "mbarriers");
+static_assert(L_FREE + 16 <= BAR_O && BAR_O + 8 <= 8 * NUM_BARS, "mbarriers");
 static_assert(SMEM_BYTES <= 232448, "227 KB of dynamic shared memory per CTA");
 static_assert(TM_XO + 128 <= TM_U && TM_U + 32 <= TM_XB && TM_XB + 16 <= TM_UB && TM_UB + 16 <= TM_G &&
-              TM_G + 80 <= TM_COLS, "TMEM columns");
+              TM_G + 80 <= TM_UL && TM_UL + 16 <= TM_COLS, "TMEM columns");
 
 struct Maps {
     CUtensorMap q, k, v, g, o;
@@ -197,12 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, const float *__restrict__ beta,
              const float *init_state, const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
              __nv_bfloat16 *__restrict__ out, float *final_state, int32_t *__restrict__ status,
-             const int32_t *__restrict__ order, float *__restrict__ out_f32) {
+             const int32_t *__restrict__ order, float *__restrict__ out_f32, const Snapshots snaps) {
     extern __shared__ uint8_t smem_raw[];
     // 1024-aligned base, derived from the shared array so accesses stay in the shared window
     uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-    const uint32_t sb = smem_u32(smem);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    // warp-uniform by construction (a shuffle from lane 0), so that the compiler
+    // keeps them, and what is derived from them, in uniform registers
+    const uint32_t sb = __shfl_sync(0xffffffffu, smem_u32(smem), 0);
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int warp = __shfl_sync(0xffffffffu, tid >> 5, 0);
     const int sp = warp & 3;          // TMEM sub-partition (lanes 32 sp .. 32 sp + 31)
     const int h = blockIdx.x;
     const int n = order ? order[blockIdx.y] : static_cast<int>(blockIdx.y);   // longest first
@@ -238,7 +245,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = misc[MISC_TMEM];
+    const uint32_t tmem = __shfl_sync(0xffffffffu, misc[MISC_TMEM], 0);
     const uint32_t tlane = tmem + ((uint32_t)(32 * sp) << 16);   // this warp's lanes
 
     auto bar = [&](uint32_t b) { return sb + OFF_BAR + b; };
@@ -337,16 +344,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             asm volatile("bar.sync 3, 256;" ::: "memory");
             if (warp == 8 && lane == 0 && x + 2 < nchunks) {
                 issue_qk(x + 2);
-                if (x + 3 < nchunks) {
-                    const int32_t y3 = (int32_t)chunk_t0(x + 3);
-                    tma_prefetch_2d(&maps.q, h * kD, y3);
-                    tma_prefetch_2d(&maps.q, h * kD + 64, y3);
-                    tma_prefetch_2d(&maps.k, h * kD, y3);
-                    tma_prefetch_2d(&maps.k, h * kD + 64, y3);
-                    tma_prefetch_2d(&maps.v, h * kD, y3);
-                    tma_prefetch_2d(&maps.v, h * kD + 64, y3);
-                    tma_prefetch_2d(&maps.g, h * kD, y3);
-                }
             }
 #pragma unroll
             for (int gi = 0; gi < 2; ++gi) {
@@ -474,22 +471,21 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             if (lane == 0) mbar_arrive(bar(FULL_B + 8 * (x % 3)));
         }
     } else if (warp == 7) {
-        // ====================================================== the Gram MMAs
-        if (lane == 0) {
-            const uint32_t id = idesc_bf16(128, 80, 0, 0);
+        // ====================================================== the Gram MMAs (one elected lane)
+        const uint32_t id = idesc_bf16(128, 80, 0, 0);
 #pragma unroll 1
-            for (int x = 0; x < nchunks; ++x) {
-                wait_bar(FULL_B + 8 * (x % 3), (x / 3) & 1);
-                if (x >= 1) wait_bar(TG_FREE, (x - 1) & 1);
-                tc_fence_after();
+        for (int x = 0; x < nchunks; ++x) {
+            wait_bar(FULL_B + 8 * (x % 3), (x / 3) & 1);
+            if (x >= 1) wait_bar(TG_FREE, (x - 1) & 1);
+            __syncwarp();
+            tc_fence_after();
+            constexpr uint64_t dk = sw128_hi(0, 1024);
 #pragma unroll
-                for (int kk = 0; kk < 8; ++kk)
-                    mma_bf16(tmem + TM_G, sw128_desc(sb + OFF_GL + (kk >> 2) * GL_HALF + (kk & 3) * 32, 0, 1024),
-                             sw128_desc(sb + OFF_R + (kk >> 2) * R_HALF + (kk & 3) * 32, 0, 1024), id, kk > 0);
-                mma_commit(bar(BAR_G));
-            }
+            for (int kk = 0; kk < 8; ++kk)
+                mma_bf16_w(tmem + TM_G, dk | sw128_lo(sb + OFF_GL + (kk >> 2) * GL_HALF + (kk & 3) * 32),
+                           dk | sw128_lo(sb + OFF_R + (kk >> 2) * R_HALF + (kk & 3) * 32), id, kk > 0);
+            mma_commit_w(bar(BAR_G));
         }
-        __syncwarp();
     } else if (warp >= 4) {
         // ====================================================== L, P, the inverse, v
         // Warp 4: k rows (L: off-diagonal block, diagonal hi.hi), then the inverse's
@@ -746,57 +742,84 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             range_bad |= !(mx <= kF16Max);
             tmem_st16_nowait(tlane + dst, y);
         };
+        // the document's next snapshot: its state after the tokens before offsets[snap]
+        int32_t snap = snaps.n > 0 ? snap_first(snaps, bos) : 0;
+        auto snap_at = [&](int64_t at) -> float * {
+            if (snap < snaps.n && static_cast<int64_t>(snaps.offsets[snap]) == at)
+                return snaps.out + (static_cast<size_t>(snap++) * H + h) * kD * kD + 32 * sp + lane;
+            return nullptr;
+        };
+        // U^T (32 columns) to fp16 high and low parts, with the range check
+        auto to_f16_hilo = [&](uint32_t src, uint32_t dst_hi, uint32_t dst_lo) {
+            float xv[32];
+            tmem_ld32(tlane + src, xv);
+            uint32_t hi[16], lo[16];
+            float mx = 0.f;
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+                mx = max_abs_nan(max_abs_nan(mx, xv[2 * e]), xv[2 * e + 1]);
+                hi[e] = pack_f16x2(xv[2 * e], xv[2 * e + 1]);
+                const float2 h2 = __half22float2(*reinterpret_cast<const __half2 *>(&hi[e]));
+                lo[e] = pack_f16x2(xv[2 * e] - h2.x, xv[2 * e + 1] - h2.y);
+            }
+            range_bad |= !(mx <= kF16Max);
+            tmem_st16_nowait(tlane + dst_hi, hi);
+            tmem_st16_nowait(tlane + dst_lo, lo);
+        };
 #pragma unroll 1
         for (int c = 0; c < nchunks; ++c) {
             if (c >= 1) wait_bar(BAR_3, (c - 1) & 1);
             wait_bar(FULL_B + 8 * (c % 3), (c / 3) & 1);
             tc_fence_after();
-            // the state's fp16 copy (the A operand of -(K+ S) and Q+ S), 64 columns a load
+            // one pass over the state, 32 columns a load: its fp16 copy (the A operand of
+            // -(K+ S) and Q+ S), then S <- Diag(e^{G_31}) S in place (before S += Khat^T U)
+            {
+                const uint32_t dvec = sb + OFF_VEC + VEC_D + (c % 3) * 512;
+                float *snap_dst = c > 0 ? snap_at(chunk_t0(c)) : nullptr;   // the state before chunk c
 #pragma unroll 1
-            for (int q2 = 0; q2 < 2; ++q2) {
-                float xs[64];
-                tmem_ld64(tlane + TM_S + 64 * q2, xs);
+                for (int q4b = 0; q4b < 4; ++q4b) {
+                    float xs[32];
+                    tmem_ld32(tlane + TM_S + 32 * q4b, xs);
+                    if (snap_dst != nullptr) {
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {
+                        for (int e = 0; e < 32; ++e) snap_dst[(size_t)(32 * q4b + e) * kD] = xs[e];
+                    }
                     uint32_t y[16];
 #pragma unroll
-                    for (int e = 0; e < 16; ++e) y[e] = pack_f16x2(xs[32 * hh + 2 * e], xs[32 * hh + 2 * e + 1]);
-                    tmem_st16_nowait(tlane + TM_SB + 32 * q2 + 16 * hh, y);
+                    for (int e = 0; e < 16; ++e) y[e] = pack_f16x2(xs[2 * e], xs[2 * e + 1]);
+                    tmem_st16_nowait(tlane + TM_SB + 16 * q4b, y);
+#pragma unroll
+                    for (int e = 0; e < 32; e += 4) {
+                        const float4 d = ld_shared_f4(dvec + 4 * (32 * q4b + e));
+                        const float2 a2 = f2mul(make_float2(xs[e], xs[e + 1]), make_float2(d.x, d.y));
+                        const float2 b2 = f2mul(make_float2(xs[e + 2], xs[e + 3]), make_float2(d.z, d.w));
+                        xs[e] = a2.x; xs[e + 1] = a2.y; xs[e + 2] = b2.x; xs[e + 3] = b2.y;
+                    }
+                    tmem_st32_nowait(tlane + TM_S + 32 * q4b, xs);
                 }
             }
             tmem_wait_st();
             if (tid == 0) bulk_wait_read_all();    // the previous output tile has been read
             tc_fence_before();
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (tid == 0) {
+            if (warp == 0) {
                 // [-(K+ S)^T | (Q+ S)^T] of chunk c
                 tc_fence_after();
                 const uint32_t id = idesc_f16(128, 64, 0, 0);
+                const uint32_t aq = sb + OFF_AQ + (c % 3) * AQ_SLOT;
+                const uint32_t dx = tmem + txo(c);
+                constexpr uint64_t dk = sw128_hi(0, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 8; ++kk)
-                    mma_tmem_a(tmem + txo(c), tmem + TM_SB + 8 * kk,
-                               sw128_desc(sb + OFF_AQ + (c % 3) * AQ_SLOT + (kk >> 2) * AQ_HALF + (kk & 3) * 32, 0, 1024),
-                               id, kk > 0);
-                mma_commit(bar(BAR_1));
+                    mma_tmem_a_w(dx, tmem + TM_SB + 8 * kk, dk | sw128_lo(aq + (kk >> 2) * AQ_HALF + (kk & 3) * 32),
+                                 id, kk > 0);
+                mma_commit_w(bar(BAR_1));
             }
             // the previous chunk's outputs, under this chunk's MMA
-            if (c >= 1) out_conv(c - 1);
-            // S <- Diag(e^{G_31}) S in place (before S += Khat^T U of this chunk)
-            {
-                const uint32_t dvec = sb + OFF_VEC + VEC_D + (c % 3) * 512;
-#pragma unroll 1
-                for (int q2 = 0; q2 < 2; ++q2) {
-                    float xs[64];
-                    tmem_ld64(tlane + TM_S + 64 * q2, xs);
-#pragma unroll
-                    for (int e = 0; e < 64; e += 4) {
-                        const float4 d = ld_shared_f4(dvec + 4 * (64 * q2 + e));
-                        const float2 a2 = f2mul(make_float2(xs[e], xs[e + 1]), make_float2(d.x, d.y));
-                        const float2 b2 = f2mul(make_float2(xs[e + 2], xs[e + 3]), make_float2(d.z, d.w));
-                        xs[e] = a2.x; xs[e + 1] = a2.y; xs[e + 2] = b2.x; xs[e + 3] = b2.y;
-                    }
-                    tmem_st64(tlane + TM_S + 64 * q2, xs);
-                }
+            if (c >= 1) {
+                wait_bar(BAR_O, (c - 1) & 1);
+                tc_fence_after();
+                out_conv(c - 1);
             }
             // -(K+ S)^T to fp16, then U = Tb V + Tb (-K+ S)
             wait_bar(BAR_1, c & 1);
@@ -805,48 +828,55 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             tmem_wait_st();
             tc_fence_before();
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (tid == 0) {
+            if (warp == 0) {
                 tc_fence_after();
                 wait_bar(TB_FULL + 8 * (c & 1), (c >> 1) & 1);
+                __syncwarp();
                 tc_fence_after();
                 const uint32_t id = idesc_f16(128, 32, 1, 0), id2 = idesc_f16(128, 32, 0, 0);
                 const uint32_t tbs = sb + OFF_TB + (c & 1) * SQ_SLOT;
+                const uint32_t vs = sb + OFF_V + (c % 3) * V_SLOT;
+                constexpr uint64_t dk = sw128_hi(0, 1024), dmn = sw128_hi(TILE_HALF, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
-                    mma_bf16(tmem + TM_U, sw128_desc(sb + OFF_V + (c % 3) * V_SLOT + kk * 2048, TILE_HALF, 1024),
-                             sw128_desc(tbs + kk * 32, 0, 1024), id, kk > 0);
+                    mma_bf16_w(tmem + TM_U, dmn | sw128_lo(vs + kk * 2048), dk | sw128_lo(tbs + kk * 32), id, kk > 0);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
-                    mma_tmem_a(tmem + TM_U, tmem + TM_XB + 8 * kk, sw128_desc(tbs + kk * 32, 0, 1024), id2, 1);
-                mma_commit(bar(BAR_2));
-                mma_commit(bar(TB_FREE + 8 * (c & 1)));
+                    mma_tmem_a_w(tmem + TM_U, tmem + TM_XB + 8 * kk, dk | sw128_lo(tbs + kk * 32), id2, 1);
+                mma_commit_w(bar(BAR_2));
+                mma_commit_w(bar(TB_FREE + 8 * (c & 1)));
             }
             // U^T to fp16, then S += Khat^T U and O += P U
             wait_bar(BAR_2, c & 1);
             tc_fence_after();
             if (tid == 0 && c + 3 < nchunks) issue_v(c + 3);   // Tb V of chunk c has read its slot
-            to_f16(TM_U, TM_UB);
+            to_f16_hilo(TM_U, TM_UB, TM_UL);
             tmem_wait_st();
             tc_fence_before();
             asm volatile("bar.sync 1, 128;" ::: "memory");
-            if (tid == 0) {
+            if (warp == 0) {
                 tc_fence_after();
                 const uint32_t is = idesc_f16(128, 128, 0, 1), io = idesc_f16(128, 32, 0, 0);
+                const uint32_t kh = sb + OFF_KH + (c % 3) * KH_SLOT, pmb = sb + OFF_PM + (c & 1) * SQ_SLOT;
+                constexpr uint64_t dk = sw128_hi(0, 1024), dmn = sw128_hi(KH_HALF, 1024);
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
-                    mma_tmem_a(tmem + TM_S, tmem + TM_UB + 8 * kk,
-                               sw128_desc(sb + OFF_KH + (c % 3) * KH_SLOT + kk * 2048, KH_HALF, 1024), is, 1);
+                    mma_tmem_a_w(tmem + TM_S, tmem + TM_UB + 8 * kk, dmn | sw128_lo(kh + kk * 2048), is, 1);
+                mma_commit_w(bar(BAR_3));   // the state first: the next chunk waits on it
 #pragma unroll
                 for (int kk = 0; kk < 2; ++kk)
-                    mma_tmem_a(tmem + txo(c) + 32, tmem + TM_UB + 8 * kk,
-                               sw128_desc(sb + OFF_PM + (c & 1) * SQ_SLOT + kk * 32, 0, 1024), io, 1);
-                mma_commit(bar(BAR_3));
-                mma_commit(bar(EMPTY_B + 8 * (c % 3)));
-                mma_commit(bar(PM_FREE + 8 * (c & 1)));
+                    mma_tmem_a_w(tmem + txo(c) + 32, tmem + TM_UB + 8 * kk, dk | sw128_lo(pmb + kk * 32), io, 1);
+#pragma unroll
+                for (int kk = 0; kk < 2; ++kk)
+                    mma_tmem_a_w(tmem + txo(c) + 32, tmem + TM_UL + 8 * kk, dk | sw128_lo(pmb + kk * 32), io, 1);
+                mma_commit_w(bar(BAR_O));
+                mma_commit_w(bar(EMPTY_B + 8 * (c % 3)));
+                mma_commit_w(bar(PM_FREE + 8 * (c & 1)));
             }
         }
         if (nchunks > 0) {
             wait_bar(BAR_3, (nchunks - 1) & 1);
+            wait_bar(BAR_O, (nchunks - 1) & 1);
             tc_fence_after();
             if (tid == 0) bulk_wait_read_all();
             asm volatile("bar.sync 1, 128;" ::: "memory");
@@ -879,16 +909,28 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                 if (misc[MISC_V + s] != 0xffffffffu)
                     mbar_wait(bar(BAR_V + 8 * s), (misc[MISC_V + s] / 3) & 1, 100000000ull);
         }
-    } else if (final_state != nullptr && warp < 4) {
-        // S^T lane v, columns i  ->  final_state[i][v]
+    } else if (warp < 4) {
+        // S^T lane v, columns i  ->  final_state[i][v], and the snapshot at the
+        // document's end when one is asked for
         const int v = 32 * sp + lane;
-        float *dst = final_state + unit * kD * kD + v;
+        float *dst = final_state != nullptr ? final_state + unit * kD * kD + v : nullptr;
+        float *sdst = nullptr;
+        if (nchunks > 0 && snaps.n > 0) {
+            const int32_t i = snap_first(snaps, eos - 1);
+            if (i < snaps.n && static_cast<int64_t>(snaps.offsets[i]) == eos)
+                sdst = snaps.out + (static_cast<size_t>(i) * H + h) * kD * kD + v;
+        }
+        if (dst != nullptr || sdst != nullptr) {
 #pragma unroll 1
-        for (int q4b = 0; q4b < 4; ++q4b) {
-            float S[32];
-            tmem_ld32(tlane + TM_S + 32 * q4b, S);
+            for (int q4b = 0; q4b < 4; ++q4b) {
+                float S[32];
+                tmem_ld32(tlane + TM_S + 32 * q4b, S);
 #pragma unroll
-            for (int e = 0; e < 32; ++e) dst[(size_t)(32 * q4b + e) * kD] = S[e];
+                for (int e = 0; e < 32; ++e) {
+                    if (dst != nullptr) dst[(size_t)(32 * q4b + e) * kD] = S[e];
+                    if (sdst != nullptr) sdst[(size_t)(32 * q4b + e) * kD] = S[e];
+                }
+            }
         }
     }
     if (tid == 0) bulk_wait_all();   // the output stores of thread 0 are complete
@@ -948,7 +990,8 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
                                  const float *beta, const float *init_state,
                                  const int32_t *cu_seqlens, int32_t N, int64_t T, int32_t H,
                                  void *out, float *final_state, int32_t *status,
-                                 cudaStream_t stream, const int32_t *order, float *out_f32) {
+                                 cudaStream_t stream, const int32_t *order, float *out_f32,
+                                 Snapshots snaps) {
     Maps maps;
     if (!make_map(&maps.q, q, T, H, false) || !make_map(&maps.k, k, T, H, false) ||
         !make_map(&maps.v, v, T, H, false) || !make_map(&maps.g, g, T, H, true) ||
@@ -959,7 +1002,7 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
     if (e != cudaSuccess) return e;
     chunk_kernel<<<dim3(H, N), kThreads, SMEM_BYTES, stream>>>(
         maps, g, beta, init_state, cu_seqlens, N, T, H, static_cast<__nv_bfloat16 *>(out),
-        final_state, status, order, out_f32);
+        final_state, status, order, out_f32, snaps);
     count_launches(1);
     return cudaGetLastError();
 }
