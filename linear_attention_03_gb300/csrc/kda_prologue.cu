@@ -110,14 +110,35 @@ __device__ __forceinline__ float2 mul2(float2 a, float2 b) {
         : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
     return *reinterpret_cast<float2 *>(&d);
 }
-// Swish s = y sigmoid(y) on a pair, y / (1 + e^-y) for either output type.
-// (The hardware tanh form 0.5 y (1 + tanh(y / 2)), one special-function op,
-// has an error of ~5e-4 of s: below bf16's rounding step, but it moves about
-// one bf16 rounding in sixteen to the neighbouring value, and the prefill
-// carries those changed inputs into every later output.)
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    unsigned long long d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d)
+        : "l"(*reinterpret_cast<unsigned long long *>(&a)), "l"(*reinterpret_cast<unsigned long long *>(&b)));
+    return *reinterpret_cast<float2 *>(&d);
+}
+__device__ __forceinline__ float ex2_approx(float x) {   // 2^x, the special-function unit
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcp_approx(float x) {   // 1/x, the special-function unit
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+// Swish s = y sigmoid(y) on a pair, y / (1 + e^-y) for either output type:
+// e^-y = 2^(-y log2 e) and the reciprocal on the special-function unit (each a
+// few fp32 ulps), the multiplies and the add paired.  (The hardware tanh form
+// 0.5 y (1 + tanh(y / 2)), one special-function op, has an error of ~5e-4 of
+// s: below bf16's rounding step, but it moves about one bf16 rounding in
+// sixteen to the neighbouring value, and the prefill carries those changed
+// inputs into every later output.)
+constexpr float kLog2e = 1.4426950408889634f;
 template <typename Tin>
 __device__ __forceinline__ float2 swish2(float2 y) {
-    return make_float2(__fdividef(y.x, 1.f + __expf(-y.x)), __fdividef(y.y, 1.f + __expf(-y.y)));
+    const float2 t = mul2(y, make_float2(-kLog2e, -kLog2e));
+    const float2 d = add2(make_float2(ex2_approx(t.x), ex2_approx(t.y)), make_float2(1.f, 1.f));
+    return mul2(y, make_float2(rcp_approx(d.x), rcp_approx(d.y)));
 }
 
 template <typename Tin, int D>
