@@ -345,10 +345,17 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             if (warp == 8 && lane == 0 && x + 2 < nchunks) {
                 issue_qk(x + 2);
             }
-#pragma unroll
+#pragma unroll 1
             for (int gi = 0; gi < 2; ++gi) {
                 const int grp = 2 * pw + gi;
                 const int chalf = grp >> 3;
+                // this group's registers, selected (the loop is not unrolled: half the code)
+                uint32_t qg[4], kg[4];
+                float gg[8];
+#pragma unroll
+                for (int m = 0; m < 4; ++m) { qg[m] = gi ? qr[1][m] : qr[0][m]; kg[m] = gi ? kr[1][m] : kr[0][m]; }
+#pragma unroll
+                for (int i = 0; i < 8; ++i) gg[i] = gi ? gnext[1][i] : gnext[0][i];
                 const uint32_t co = sw128_off(lane, grp & 7);
                 // G in log2 units per token pair: pair sums, a prefix over the quad
                 // (the 8 tokens of a matrix), group totals
@@ -358,7 +365,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                     float O = 0.f;
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
-                        const float2 gp = f2mul(make_float2(gnext[gi][2 * m], gnext[gi][2 * m + 1]),
+                        const float2 gp = f2mul(make_float2(gg[2 * m], gg[2 * m + 1]),
                                                 make_float2(kLog2e, kLog2e));
                         float xs = gp.x + gp.y;
                         float ys = __shfl_up_sync(0xffffffffu, xs, 1, 4);
@@ -383,7 +390,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                 for (int m = 0; m < 4; ++m) {
                     const int a = m >> 1;                      // 16-token tile
                     const float sa = a ? e0 : 0.f, ea = a ? e1 : e0;
-                    float2 k2 = unpack_bf16x2(kr[gi][m]), q2 = unpack_bf16x2(qr[gi][m]);
+                    float2 k2 = unpack_bf16x2(kg[m]), q2 = unpack_bf16x2(qg[m]);
                     if (!full) {
                         const int t0k = 8 * m + 2 * q4;
                         if (t0k >= lenx) { k2.x = 0.f; q2.x = 0.f; }
