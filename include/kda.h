@@ -122,6 +122,12 @@ KDA_API size_t kda_prefill_workspace_size(kda_dims dims, int64_t T, int32_t N);
  *              are the same either way.
  * g is used as given; the tensor-core path relies on g >= -5 per token (the
  * bounded gate) to keep its 16-token rescaling factors inside fp32 range.
+ * The tensor-core path (bf16, d = 128) keeps v, the state and the
+ * pseudo-values in fp16 operands: a magnitude of 65504 or more (or a NaN)
+ * there sets KDA_DEVICE_RANGE in the status word, and the results of that
+ * call are then not valid.  Outputs match the exact recurrence per element
+ * within 2e-2 of their RMS plus their own bf16 rounding; final states within
+ * 2e-2 of their RMS.
  * T = 0 is allowed (final_state = init_state).
  */
 KDA_API kda_status kda_prefill(const void *q, const void *k, const void *v,
