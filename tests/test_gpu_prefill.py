@@ -169,3 +169,25 @@ def test_gate_at_its_bound(kda):
     ref_out, ref_fin = oracle_prefill(inp)
     compare(out, ref_out, torch.bfloat16, "gate at its bound, out")
     compare(fin, ref_fin, torch.bfloat16, "gate at its bound, state")
+
+
+@pytest.mark.parametrize("where", ["v", "state"])
+def test_fp16_operand_range_is_reported(kda, where):
+    """The tensor-core path keeps v and the state in fp16 operands: a value at
+    or beyond fp16's largest finite magnitude sets KDA_DEVICE_RANGE in the
+    status word (inputs of ordinary size leave it clear)."""
+    T, H, d = 96, 2, 128
+    inp = to_device(synth.custom(T, H, d, torch.bfloat16, seed=980, init_std=0.05))
+    init = inp["init_state"].clone()
+    v = inp["v"].clone()
+    if where == "v":
+        v[40, 1, 7] = 7.0e4                      # one value of v past 65504
+    else:
+        init[0, 0, 3, 5] = 7.0e4                 # one state entry past 65504
+    ws = torch.empty(256, dtype=torch.uint8, device="cuda")
+    kda.kda_prefill(inp["q"], inp["k"], v, inp["g"], inp["beta"], init, workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_RANGE
+    kda.kda_prefill(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["init_state"], workspace=ws)
+    torch.cuda.synchronize()
+    assert kda.kda_get_device_status(ws) == kda.KDA_DEVICE_OK
