@@ -58,3 +58,24 @@ def test_pipeline_empty_document_keeps_the_state(kda):
                                         torch.empty(0, 2, device="cuda"), s0, 64)
     assert out.numel() == 0
     assert torch.equal(fin, s0)
+
+
+def test_pipeline_streams_belong_to_the_caller(kda):
+    """The prefills run on the caller's stream and the prologues on the
+    caller's second stream; the same stream for both runs the segments one
+    after another. Either way the results are the same bit for bit, and the
+    caller's stream holds the end of the call."""
+    raw = to_device(synth.custom_raw(1000, 2, 128, torch.bfloat16, seed=1190))
+    args = (raw["q_raw"], raw["k_raw"], raw["v_raw"], raw["conv_w"], raw["z_g"], raw["z_beta"], None, 256)
+    main = torch.cuda.Stream(priority=-1)
+    side = torch.cuda.Stream(priority=0)
+    with torch.cuda.stream(main):
+        out_o, fin_o = kda.kda_prologue_prefill(*args, prologue_stream=side)
+        done = torch.cuda.Event()
+        done.record()
+    done.synchronize()                   # the caller's stream alone orders the results
+    out_o, fin_o = out_o.clone(), fin_o.clone()
+    with torch.cuda.stream(main):
+        out_s, fin_s = kda.kda_prologue_prefill(*args, prologue_stream=main)
+    torch.cuda.synchronize()
+    assert torch.equal(out_o, out_s) and torch.equal(fin_o, fin_s)
