@@ -41,17 +41,20 @@
 //   warps 8..15  the operand pass of chunk x + 2: q, k by ldmatrix, g by
 //                loads a chunk ahead; a lane owns one channel and two
 //                consecutive tokens; every decay-scaled operand out by a
-//                transposed stmatrix (two 8-channel groups per warp)
+//                transposed stmatrix (two 8-channel groups per warp, as a
+//                loop).  Warps 12..15 also take the second half (key
+//                channels 64..127) of the chain's state pass
 //   warp 7       the Gram MMA of chunk x + 1
 //   warps 4..6   chunk x + 1's L and P out of TMEM, the 32 x 32 inverse (warp 4:
 //                the diagonal blocks; warp 5: the off-diagonal block, a chunk
 //                behind), v to fp16 (warp 6)
-//   warps 0..3   the state chain of chunk x: the state's fp16 copy, -(K+ S)
-//                and Q+ S, Tb V + Tb (-K+ S), S += Khat^T U and O += P U, the
-//                outputs of chunk x - 1 out under chunk x's first MMA
+//   warps 0..3   the state chain of chunk x: the state's fp16 copy and its
+//                decay (first half; see warps 12..15), -(K+ S) and Q+ S,
+//                Tb V + Tb (-K+ S), S += Khat^T U and O += P U, the outputs of
+//                chunk x - 1 out under chunk x's first MMA
 // Prefix snapshots (every offset 64 tokens into a document, or its end) are
-// written by the chain warps from the state's fp32 TMEM copy as they read it
-// at the top of a chunk, and at the end.
+// written from the state's fp32 TMEM copy by the warps of the state pass as
+// they read it at the top of a chunk, and by the chain warps at the end.
 // All waits are bounded: a lost arrival sets KDA_DEVICE_TIMEOUT, every later
 // wait of the CTA returns at once, and the CTA leaves after draining its own
 // outstanding copies and MMAs.
@@ -305,6 +308,39 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
     __syncthreads();
     tc_fence_after();
 
+    // The state pass over the 32-column pieces [q0, q1) of chunk c: the fp16 copy
+    // of the state (the A operand of -(K+ S) and Q+ S), then S <- Diag(e^{G_31}) S
+    // in place (before S += Khat^T U); the state before chunk c goes to a
+    // snapshot when one is asked for.  Pieces 0-1 by the chain warps, 2-3 by
+    // warps 12..15 (each warp its own 32 lanes).
+    auto state_pass = [&](int c, int q0, int q1, int32_t &snap) {
+        const uint32_t dvec = sb + OFF_VEC + VEC_D + (c % 3) * 512;
+        float *snap_dst = nullptr;
+        if (c > 0 && snap < snaps.n && static_cast<int64_t>(snaps.offsets[snap]) == chunk_t0(c))
+            snap_dst = snaps.out + (static_cast<size_t>(snap++) * H + h) * kD * kD + 32 * sp + lane;
+#pragma unroll 1
+        for (int q4b = q0; q4b < q1; ++q4b) {
+            float xs[32];
+            tmem_ld32(tlane + TM_S + 32 * q4b, xs);
+            if (snap_dst != nullptr) {
+#pragma unroll
+                for (int e = 0; e < 32; ++e) snap_dst[(size_t)(32 * q4b + e) * kD] = xs[e];
+            }
+            uint32_t y[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) y[e] = pack_f16x2(xs[2 * e], xs[2 * e + 1]);
+            tmem_st16_nowait(tlane + TM_SB + 16 * q4b, y);
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+                const float4 d = ld_shared_f4(dvec + 4 * (32 * q4b + e));
+                const float2 a2 = f2mul(make_float2(xs[e], xs[e + 1]), make_float2(d.x, d.y));
+                const float2 b2 = f2mul(make_float2(xs[e + 2], xs[e + 3]), make_float2(d.z, d.w));
+                xs[e] = a2.x; xs[e + 1] = a2.y; xs[e + 2] = b2.x; xs[e + 3] = b2.y;
+            }
+            tmem_st32_nowait(tlane + TM_S + 32 * q4b, xs);
+        }
+    };
+
     if (warp >= 8) {
         // ====================================================== operand pass
         // two 8-channel groups per warp; a lane owns channel 8 grp + lane / 4 and
@@ -325,10 +361,23 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             }
         };
         if (nchunks > 0) load_g(0);
+        // warps 12..15: the second half of chunk c's state pass, beside the chain's
+        int32_t hsnap = snaps.n > 0 ? snap_first(snaps, bos) : 0;
+        auto help = [&](int c) {
+            if (c >= 1) wait_bar(BAR_3, (c - 1) & 1);
+            wait_bar(FULL_B + 8 * (c % 3), (c / 3) & 1);
+            __syncwarp();
+            tc_fence_after();
+            state_pass(c, 2, 4, hsnap);
+            tmem_wait_st();
+            tc_fence_before();
+            asm volatile("bar.sync 5, 256;" ::: "memory");
+        };
 #pragma unroll 1
         for (int x = 0; x < nchunks; ++x) {
             const int lenx = chunk_len(x);
             const bool full = lenx == kC;
+            if (warp >= 12 && x >= 2) help(x - 2);
             wait_bar(BAR_QK + 8 * (x & 1), (x >> 1) & 1);
             uint32_t qr[2][4], kr[2][4];
 #pragma unroll
@@ -476,6 +525,10 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             fence_proxy_async();
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(FULL_B + 8 * (x % 3)));
+        }
+        if (warp >= 12) {
+#pragma unroll 1
+            for (int c = nchunks > 2 ? nchunks - 2 : 0; c < nchunks; ++c) help(c);
         }
     } else if (warp == 7) {
         // ====================================================== the Gram MMAs (one elected lane)
@@ -751,11 +804,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
         };
         // the document's next snapshot: its state after the tokens before offsets[snap]
         int32_t snap = snaps.n > 0 ? snap_first(snaps, bos) : 0;
-        auto snap_at = [&](int64_t at) -> float * {
-            if (snap < snaps.n && static_cast<int64_t>(snaps.offsets[snap]) == at)
-                return snaps.out + (static_cast<size_t>(snap++) * H + h) * kD * kD + 32 * sp + lane;
-            return nullptr;
-        };
         // U^T (32 columns) to fp16 high and low parts, with the range check
         auto to_f16_hilo = [&](uint32_t src, uint32_t dst_hi, uint32_t dst_lo) {
             float xv[32];
@@ -778,37 +826,11 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             if (c >= 1) wait_bar(BAR_3, (c - 1) & 1);
             wait_bar(FULL_B + 8 * (c % 3), (c / 3) & 1);
             tc_fence_after();
-            // one pass over the state, 32 columns a load: its fp16 copy (the A operand of
-            // -(K+ S) and Q+ S), then S <- Diag(e^{G_31}) S in place (before S += Khat^T U)
-            {
-                const uint32_t dvec = sb + OFF_VEC + VEC_D + (c % 3) * 512;
-                float *snap_dst = c > 0 ? snap_at(chunk_t0(c)) : nullptr;   // the state before chunk c
-#pragma unroll 1
-                for (int q4b = 0; q4b < 4; ++q4b) {
-                    float xs[32];
-                    tmem_ld32(tlane + TM_S + 32 * q4b, xs);
-                    if (snap_dst != nullptr) {
-#pragma unroll
-                        for (int e = 0; e < 32; ++e) snap_dst[(size_t)(32 * q4b + e) * kD] = xs[e];
-                    }
-                    uint32_t y[16];
-#pragma unroll
-                    for (int e = 0; e < 16; ++e) y[e] = pack_f16x2(xs[2 * e], xs[2 * e + 1]);
-                    tmem_st16_nowait(tlane + TM_SB + 16 * q4b, y);
-#pragma unroll
-                    for (int e = 0; e < 32; e += 4) {
-                        const float4 d = ld_shared_f4(dvec + 4 * (32 * q4b + e));
-                        const float2 a2 = f2mul(make_float2(xs[e], xs[e + 1]), make_float2(d.x, d.y));
-                        const float2 b2 = f2mul(make_float2(xs[e + 2], xs[e + 3]), make_float2(d.z, d.w));
-                        xs[e] = a2.x; xs[e + 1] = a2.y; xs[e + 2] = b2.x; xs[e + 3] = b2.y;
-                    }
-                    tmem_st32_nowait(tlane + TM_S + 32 * q4b, xs);
-                }
-            }
+            state_pass(c, 0, 2, snap);   // the first half; warps 12..15 take the second
             tmem_wait_st();
             if (tid == 0) bulk_wait_read_all();    // the previous output tile has been read
             tc_fence_before();
-            asm volatile("bar.sync 1, 128;" ::: "memory");
+            asm volatile("bar.sync 5, 256;" ::: "memory");   // both halves of the state pass
             if (warp == 0) {
                 // [-(K+ S)^T | (Q+ S)^T] of chunk c
                 tc_fence_after();
