@@ -41,9 +41,10 @@
 //   warps 8..15  the operand pass of chunk x + 2: q, k by ldmatrix, g by
 //                loads a chunk ahead; a lane owns one channel and two
 //                consecutive tokens; every decay-scaled operand out by a
-//                transposed stmatrix (two 8-channel groups per warp, as a
-//                loop).  Warps 12..15 also take the second half (key
-//                channels 64..127) of the chain's state pass
+//                transposed stmatrix (8-channel groups as a loop: three per
+//                warp on warps 8..11, one on warps 12..15).  Warps 12..15
+//                also take the second half (key channels 64..127) of the
+//                chain's state pass
 //   warp 7       the Gram MMA of chunk x + 1
 //   warps 4..6   chunk x + 1's L and P out of TMEM, the 32 x 32 inverse (warp 4:
 //                the diagonal blocks; warp 5: the off-diagonal block, a chunk
@@ -343,16 +344,20 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
 
     if (warp >= 8) {
         // ====================================================== operand pass
-        // two 8-channel groups per warp; a lane owns channel 8 grp + lane / 4 and
-        // tokens 8 m + 2 (lane & 3) + {0, 1} (m = 0..3) of each group
+        // 8-channel groups: warps 8..11 take three each (0..11), warps 12..15 one
+        // each (12..15), so that the helpers are free early for the state pass.
+        // A lane owns channel 8 grp + lane / 4 and tokens 8 m + 2 (lane & 3) + {0, 1}
+        // (m = 0..3) of each group
         const int pw = warp - 8, q4 = lane & 3;
-        float gnext[2][8];
+        const int ng = pw < 4 ? 3 : 1, gb = pw < 4 ? 3 * pw : 8 + pw;
+        float gnext[3][8];
         auto load_g = [&](int x) {
             const int64_t t0 = chunk_t0(x);
             const int lc = chunk_len(x);
 #pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
-                const float *gp = g + h * kD + 8 * (2 * pw + gi) + (lane >> 2);
+            for (int gi = 0; gi < 3; ++gi) {
+                if (gi >= ng) break;
+                const float *gp = g + h * kD + 8 * (gb + gi) + (lane >> 2);
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
                     const int tk = 8 * (i >> 1) + 2 * q4 + (i & 1);
@@ -379,32 +384,21 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
             const bool full = lenx == kC;
             if (warp >= 12 && x >= 2) help(x - 2);
             wait_bar(BAR_QK + 8 * (x & 1), (x >> 1) & 1);
-            uint32_t qr[2][4], kr[2][4];
-#pragma unroll
-            for (int gi = 0; gi < 2; ++gi) {
-                const int grp = 2 * pw + gi;
-                const uint32_t a = sb + OFF_QK + (x & 1) * QK_SLOT + (grp >> 3) * TILE_HALF +
-                                   sw128_off(lane, grp & 7);
-                ldsm_x4_trans(a, qr[gi]);
-                ldsm_x4_trans(a + K_IN_SLOT, kr[gi]);
-            }
-            // every pass warp has read the slot: refill it with chunk x + 2
-            fence_proxy_async();
-            asm volatile("bar.sync 3, 256;" ::: "memory");
-            if (warp == 8 && lane == 0 && x + 2 < nchunks) {
-                issue_qk(x + 2);
-            }
 #pragma unroll 1
-            for (int gi = 0; gi < 2; ++gi) {
-                const int grp = 2 * pw + gi;
+            for (int gi = 0; gi < ng; ++gi) {
+                const int grp = gb + gi;
                 const int chalf = grp >> 3;
-                // this group's registers, selected (the loop is not unrolled: half the code)
+                // this group's q, k (ldmatrix) and gates (selected from the prefetch)
                 uint32_t qg[4], kg[4];
+                {
+                    const uint32_t a = sb + OFF_QK + (x & 1) * QK_SLOT + (grp >> 3) * TILE_HALF +
+                                       sw128_off(lane, grp & 7);
+                    ldsm_x4_trans(a, qg);
+                    ldsm_x4_trans(a + K_IN_SLOT, kg);
+                }
                 float gg[8];
 #pragma unroll
-                for (int m = 0; m < 4; ++m) { qg[m] = gi ? qr[1][m] : qr[0][m]; kg[m] = gi ? kr[1][m] : kr[0][m]; }
-#pragma unroll
-                for (int i = 0; i < 8; ++i) gg[i] = gi ? gnext[1][i] : gnext[0][i];
+                for (int i = 0; i < 8; ++i) gg[i] = gi == 0 ? gnext[0][i] : (gi == 1 ? gnext[1][i] : gnext[2][i]);
                 const uint32_t co = sw128_off(lane, grp & 7);
                 // G in log2 units per token pair: pair sums, a prefix over the quad
                 // (the 8 tokens of a matrix), group totals
@@ -428,7 +422,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                     }
                     e1 = O;   // G after tile 0 (= s_1) and after tile 1 (= G_31)
                 }
-                if (gi == 1 && x + 1 < nchunks) load_g(x + 1);   // the next chunk's gates, a chunk ahead
+                if (gi == ng - 1 && x + 1 < nchunks) load_g(x + 1);   // the next chunk's gates, a chunk ahead
                 const float fd0 = ex2(-e0), fd1 = ex2(e0 - e1);   // e^{s_a - e_a}, diagonal right rows
                 const float gs1 = ex2(e0);                         // e^{s_1}: K+ and Q+ of tile 1
                 const float kh0 = ex2(e1 - e0);                    // e^{G_31 - e_0}: Khat of tile 0
@@ -522,7 +516,10 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                     stsm_x4_trans(sb + OFF_KH + (x % 3) * KH_SLOT + chalf * KH_HALF + co, w[0], w[1], w[2], w[3]);
                 }
             }
+            // every pass warp has read the q/k slot: refill it with chunk x + 2
             fence_proxy_async();
+            asm volatile("bar.sync 3, 256;" ::: "memory");
+            if (warp == 8 && lane == 0 && x + 2 < nchunks) issue_qk(x + 2);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(FULL_B + 8 * (x % 3)));
         }
