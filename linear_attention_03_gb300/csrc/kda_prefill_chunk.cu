@@ -45,7 +45,8 @@
 //                warp on warps 8..11, one on warps 12..15).  Warps 12..15
 //                also take the second half (key channels 64..127) of the
 //                chain's state pass
-//   warp 7       the Gram MMA of chunk x + 1
+//   warp 7       the Gram MMA of chunk x + 1, then the q/k load of chunk x + 3
+//                into the slot that chunk x + 1's pass has read
 //   warps 4..6   chunk x + 1's L and P out of TMEM, the 32 x 32 inverse (warp 4:
 //                the diagonal blocks; warp 5: the off-diagonal block, a chunk
 //                behind), v to fp16 (warp 6)
@@ -516,10 +517,9 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                     stsm_x4_trans(sb + OFF_KH + (x % 3) * KH_SLOT + chalf * KH_HALF + co, w[0], w[1], w[2], w[3]);
                 }
             }
-            // every pass warp has read the q/k slot: refill it with chunk x + 2
+            // this chunk's operands are stored and its q/k slot is read (the Gram
+            // warp refills the slot with chunk x + 2 once all eight warps are here)
             fence_proxy_async();
-            asm volatile("bar.sync 3, 256;" ::: "memory");
-            if (warp == 8 && lane == 0 && x + 2 < nchunks) issue_qk(x + 2);
             __syncwarp();
             if (lane == 0) mbar_arrive(bar(FULL_B + 8 * (x % 3)));
         }
@@ -542,6 +542,9 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
                 mma_bf16_w(tmem + TM_G, dk | sw128_lo(sb + OFF_GL + (kk >> 2) * GL_HALF + (kk & 3) * 32),
                            dk | sw128_lo(sb + OFF_R + (kk >> 2) * R_HALF + (kk & 3) * 32), id, kk > 0);
             mma_commit_w(bar(BAR_G));
+            // every pass warp has read chunk x's q/k slot (FULL_B): load chunk x + 2 into it
+            if (lane == 0 && x + 2 < nchunks && !misc[MISC_ABORT]) issue_qk(x + 2);
+            __syncwarp();
         }
     } else if (warp >= 4) {
         // ====================================================== L, P, the inverse, v
