@@ -331,7 +331,8 @@ KDA_API kda_status kda_output_gate(const void *o, const void *z, const float *we
                                    kda_dims dims, float eps, void *y, void *stream);
 
 /*
- * Diagnostic of the bounded device-side waits (the paper has no counterpart).
+ * Diagnostic of the bounded device-side waits (the method's sources have no
+ * counterpart).
  * Every wait of the tensor-core prefill gives up after a time limit,
  * records KDA_DEVICE_TIMEOUT in the workspace status word and lets its CTA
  * leave, instead of hanging.  This call launches one CTA that waits on a
@@ -357,8 +358,8 @@ KDA_API const char *kda_last_error(void);
  * kda_prefill for callers that cannot allocate device memory: code embedded
  * in an engine that owns every byte of device memory, or a serving loop that
  * must not allocate once it has started, has no way to provide kda_prefill's
- * workspace.  The paper has no counterpart to this entry point; it is a
- * deployment convenience, not part of KDA.
+ * workspace.  The method's sources have no counterpart to this entry point;
+ * it is a deployment convenience, not part of KDA.
  * Same arguments and results as kda_prefill, minus the workspace: the
  * library keeps a fixed 64 KiB scratch array in device memory per GPU
  * (held until the process exits) and passes it as the workspace.  Up to
