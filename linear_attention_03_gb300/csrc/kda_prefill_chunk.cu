@@ -202,13 +202,15 @@ __device__ __forceinline__ float max_abs_nan(float m, float x) {
     return r;
 }
 
-// kPlain: no prefix snapshots and bf16 outputs, so that those paths are not in its code
-template <bool kPlain>
+// kMode 0: every option; 1: no prefix snapshots and bf16 outputs, so that those
+// paths are not in its code; 2: as 1, for one document of whole chunks
+template <int kMode>
 __global__ void __launch_bounds__(kThreads, 1)
 chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, const float *__restrict__ beta,
              const float *init_state, const int32_t *__restrict__ cu, int32_t N, int64_t T, int32_t H,
              __nv_bfloat16 *__restrict__ out, float *final_state, int32_t *__restrict__ status,
              const int32_t *__restrict__ order, float *__restrict__ out_f32_arg, const Snapshots snaps_arg) {
+    constexpr bool kPlain = kMode >= 1, kWhole = kMode == 2;
     float *const out_f32 = kPlain ? nullptr : out_f32_arg;
     Snapshots snaps = snaps_arg;
     if (kPlain) snaps.n = 0;
@@ -266,6 +268,7 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
     };
     auto chunk_t0 = [&](int x) { return bos + (int64_t)x * kC; };
     auto chunk_len = [&](int x) {
+        if (kWhole) return kC;
         const int64_t r = eos - chunk_t0(x);
         return r < kC ? static_cast<int>(r) : kC;
     };
@@ -1031,19 +1034,15 @@ cudaError_t launch_prefill_chunk(const void *q, const void *k, const void *v, co
         !make_map(&maps.v, v, T, H, false) || !make_map(&maps.g, g, T, H, true) ||
         !make_map(&maps.o, out, T, H, false))
         return cudaErrorInvalidValue;
-    static std::atomic<uint64_t> smem_set{0}, smem_set_p{0};
-    const bool plain = snaps.n == 0 && out_f32 == nullptr;
-    cudaError_t e = plain ? allow_dynamic_smem(chunk_kernel<true>, SMEM_BYTES, smem_set_p)
-                          : allow_dynamic_smem(chunk_kernel<false>, SMEM_BYTES, smem_set);
+    static std::atomic<uint64_t> smem_set[3] = {};
+    const int mode = !(snaps.n == 0 && out_f32 == nullptr) ? 0
+                     : (N == 1 && cu_seqlens == nullptr && T % kC == 0) ? 2 : 1;
+    auto kern = mode == 0 ? chunk_kernel<0> : mode == 1 ? chunk_kernel<1> : chunk_kernel<2>;
+    cudaError_t e = allow_dynamic_smem(kern, SMEM_BYTES, smem_set[mode]);
     if (e != cudaSuccess) return e;
-    if (plain)
-        chunk_kernel<true><<<dim3(H, N), kThreads, SMEM_BYTES, stream>>>(
-            maps, g, beta, init_state, cu_seqlens, N, T, H, static_cast<__nv_bfloat16 *>(out),
-            final_state, status, order, out_f32, snaps);
-    else
-        chunk_kernel<false><<<dim3(H, N), kThreads, SMEM_BYTES, stream>>>(
-            maps, g, beta, init_state, cu_seqlens, N, T, H, static_cast<__nv_bfloat16 *>(out),
-            final_state, status, order, out_f32, snaps);
+    kern<<<dim3(H, N), kThreads, SMEM_BYTES, stream>>>(
+        maps, g, beta, init_state, cu_seqlens, N, T, H, static_cast<__nv_bfloat16 *>(out),
+        final_state, status, order, out_f32, snaps);
     count_launches(1);
     return cudaGetLastError();
 }
