@@ -57,6 +57,31 @@ def test_all_documents_empty(kda):
     assert out.numel() == 0 and torch.equal(fin, s0)
 
 
+@pytest.mark.parametrize("T", [64, 96, 4096, 4100, 37])
+def test_kernel_instantiations_agree(kda, T):
+    """The tensor-core prefill is compiled three times (every option; no
+    snapshots or fp32 outputs; one document of whole chunks) and the launcher
+    picks the narrowest that fits the call.  The three give the same bits: a
+    call without offsets (the whole-chunk one when T is a multiple of 32), one
+    with offsets (the general one) and one with a snapshot at the document's
+    end (every option)."""
+    inp = synth.custom(T, 4, 128, torch.bfloat16, seed=990 + T, init_std=0.05)
+    dv = to_device(inp)
+    a_out, a_fin = kda.kda_prefill(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], dv["init_state"], None)
+    b_out, b_fin = gpu_prefill(kda, dv)
+    cu = torch.as_tensor(inp["cu_seqlens"], dtype=torch.int32, device="cuda")
+    off = torch.tensor([T], dtype=torch.int32, device="cuda")
+    c_out, c_fin, snaps = kda.kda_prefill_snapshots(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], off,
+                                                    dv["init_state"], cu)
+    torch.cuda.synchronize()
+    assert torch.equal(a_out, b_out) and torch.equal(a_fin, b_fin)
+    assert torch.equal(c_out, b_out) and torch.equal(c_fin, b_fin)
+    assert torch.equal(snaps[0], c_fin[0])
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(a_out, ref_out, torch.bfloat16, f"out T={T}")
+    compare(a_fin, ref_fin, torch.bfloat16, f"state T={T}")
+
+
 def test_split_run_carries_state(kda):
     """prefill(T1) then prefill(T2) from its final state == prefill(T1+T2)."""
     inp = to_device(synth.custom(300, 2, 128, torch.bfloat16, seed=502, init_std=0.05))

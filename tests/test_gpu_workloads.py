@@ -31,6 +31,21 @@ def test_workload2_single_sequence(kda):
     compare(fin, ref_fin, torch.bfloat16, "w2 state")
 
 
+def test_workload2_as_benchmarked(kda):
+    """The headline call as the benchmark makes it, without offsets (one
+    document of whole chunks: the kernel's narrowest instantiation), against
+    the oracle, and bit-identical to the call with offsets (the general one)."""
+    inp = synth.inputs(2)
+    dv = to_device(inp)
+    out, fin = kda.kda_prefill(dv["q"], dv["k"], dv["v"], dv["g"], dv["beta"], dv.get("init_state"), None)
+    ref_out, ref_fin = oracle_prefill(inp)
+    compare(out, ref_out, torch.bfloat16, "w2 out (no offsets)")
+    compare(fin, ref_fin, torch.bfloat16, "w2 state (no offsets)")
+    out_c, fin_c = gpu_prefill(kda, dv)
+    torch.cuda.synchronize()
+    assert torch.equal(out, out_c) and torch.equal(fin, fin_c)
+
+
 def test_workload3_packed_documents(kda):
     heads = [0, 41, 95]
     dev = synth.inputs(3, device="cuda")
