@@ -194,16 +194,6 @@ __device__ __forceinline__ void gemm16(float (&acc)[2][4], const float *A, int s
     }
 }
 
-// one test of an mbarrier phase, without waiting
-__device__ __forceinline__ bool mbar_done(uint32_t bar, uint32_t parity) {
-    uint32_t done;
-    asm volatile(
-        "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        "selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(done) : "r"(bar), "r"(parity) : "memory");
-    return done != 0;
-}
-
 // running max of |x| that keeps a NaN (an fp16 overflow anywhere upstream of
 // -K+ S or U reaches them as an infinity or a NaN)
 __device__ __forceinline__ float max_abs_nan(float m, float x) {
@@ -273,9 +263,6 @@ chunk_kernel(const __grid_constant__ Maps maps, const float *__restrict__ g, con
     auto bar = [&](uint32_t b) { return sb + OFF_BAR + b; };
     // a bounded wait that gives up at once after any earlier wait of the CTA gave up
     auto wait_bar = [&](uint32_t b, uint32_t parity) {
-        // a phase already complete returns before the abort flag is read (measured
-        // faster for the general instantiations, slower for the whole-chunk one)
-        if (!kWhole && mbar_done(sb + OFF_BAR + b, parity)) return;
         if (misc[MISC_ABORT]) return;
         if (!mbar_wait(sb + OFF_BAR + b, parity)) misc[MISC_ABORT] = 1;
     };
